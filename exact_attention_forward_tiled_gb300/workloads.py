@@ -1,0 +1,150 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module holds the shapes, seeds and random draws only; none of the
+method's arithmetic. Both the CUDA path and the oracle consume what it makes.
+
+The pages benchmark unspecified synthetic shapes ("Flash Attention 3
+principles (guijiagi)" section 4.2 table: causal 4K/8K/16K and full 8K; the
+FlashAttention-3 wiki's hdim-128/256 figures). The workloads below stand in
+for them: Q, K, V i.i.d. N(0, 1) drawn in fp32 and cast to the input dtype.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str            # "fp16" | "bf16" | "fp8"  (fp8: bf16 inputs, e4m3 compute)
+    B: int                # sequences (fixed length) or number of varlen sequences
+    H: int
+    Sq: int               # fixed: query length; varlen: max length
+    Sk: int
+    D: int
+    causal: bool
+    seed: int
+    varlen: bool = False
+    len_range: tuple = (128, 8192)   # varlen: inclusive uniform range of lengths
+    outliers: bool = False           # fp8 outlier workload
+    note: str = field(default="", compare=False)
+
+
+WORKLOADS = {
+    "c1": Workload("fp16_B1_H2_S256_D64", "fp16", 1, 2, 256, 256, 64, False, 0,
+                   note="fp16 B=1 H=2 Sq=Sk=256 D=64 non-causal, scale 1/sqrt(D), seed 0"),
+    "c2": Workload("bf16_B4_H16_S8192_D128", "bf16", 4, 16, 8192, 8192, 128, False, 1,
+                   note="bf16 B=4 H=16 Sq=Sk=8192 D=128 non-causal"),
+    "c3a": Workload("bf16_causal_B2_H16_S16384_D128", "bf16", 2, 16, 16384, 16384, 128, True, 2,
+                    note="bf16 causal B=2 H=16 Sq=Sk=16384 D=128"),
+    "c3b": Workload("bf16_causal_B1_H8_S16384_D256", "bf16", 1, 8, 16384, 16384, 256, True, 3,
+                    note="bf16 causal B=1 H=8 Sq=Sk=16384 D=256"),
+    "c4": Workload("bf16_varlen_causal_32seq_H32_D128", "bf16", 32, 32, 8192, 8192, 128, True, 4,
+                   varlen=True, note="bf16 varlen causal, 32 sequences of U[128, 8192] tokens, H=32 D=128"),
+    "c5": Workload("fp8_B4_H16_S8192_D128_outliers", "fp8", 4, 16, 8192, 8192, 128, False, 5,
+                   outliers=True,
+                   note="fp8 e4m3 B=4 H=16 Sq=Sk=8192 D=128 non-causal, block scales + Hadamard, "
+                        "0.1% N(0,10^2) outliers in 4 fixed columns"),
+}
+
+TORCH_DTYPE = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def varlen_lengths(w: Workload, device="cpu") -> torch.Tensor:
+    """Sequence lengths, i.i.d. uniform on ``len_range`` (inclusive), drawn
+    first from the workload's seed on the CPU (so both machines agree)."""
+    g = _gen(w.seed, "cpu")
+    lo, hi = w.len_range
+    return torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64)
+
+
+def cu_seqlens(lengths: torch.Tensor) -> torch.Tensor:
+    """int32 prefix sums [0, L0, L0+L1, ...]."""
+    out = torch.zeros(lengths.numel() + 1, dtype=torch.int64)
+    out[1:] = torch.cumsum(lengths.to(torch.int64), 0)
+    return out.to(torch.int32)
+
+
+def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
+    """Q, K, V of the workload as ``[tokens, H, D]`` tensors on ``device``.
+
+    Returns a dict with q, k, v, cu_seqlens_q/k (None unless varlen), the
+    lengths and, for the FP8 workload, sigma (int8 +-1 of length D) and the
+    outlier columns. Random numbers come from a ``torch.Generator`` on
+    ``device`` seeded with the workload's seed.
+    """
+    seed = w.seed if seed is None else seed
+    dt = TORCH_DTYPE[w.dtype]
+    out = {"cu_seqlens_q": None, "cu_seqlens_k": None}
+    if w.varlen:
+        lens = varlen_lengths(replace(w, seed=seed))
+        cu = cu_seqlens(lens)
+        out["lengths"] = lens
+        out["cu_seqlens_q"] = cu.to(device)
+        out["cu_seqlens_k"] = cu.to(device)
+        out["max_seqlen"] = int(lens.max())
+        Tq = Tk = int(cu[-1])
+    else:
+        Tq, Tk = w.B * w.Sq, w.B * w.Sk
+    g = _gen(seed, device)
+    q = torch.randn((Tq, w.H, w.D), generator=g, device=device, dtype=torch.float32)
+    k = torch.randn((Tk, w.H, w.D), generator=g, device=device, dtype=torch.float32)
+    v = torch.randn((Tk, w.H, w.D), generator=g, device=device, dtype=torch.float32)
+    if w.outliers:
+        # 4 distinct feature columns shared by Q, K, V and every head; in each
+        # tensor round(0.001 * numel) entries of those columns, chosen
+        # uniformly without replacement, become N(0, 10^2) draws.
+        cols = torch.randperm(w.D, generator=g, device=device)[:4]
+        out["outlier_cols"] = cols.cpu()
+        for t in (q, k, v):
+            n_out = int(round(0.001 * t.numel()))
+            cand = t.shape[0] * t.shape[1] * 4
+            pick = torch.randperm(cand, generator=g, device=device)[:n_out]
+            col = cols[pick % 4]
+            rest = pick // 4
+            head = rest % t.shape[1]
+            tok = rest // t.shape[1]
+            t[tok, head, col] = 10.0 * torch.randn((n_out,), generator=g, device=device)
+    if w.dtype == "fp8":
+        sig = torch.randint(0, 2, (w.D,), generator=g, device=device, dtype=torch.int32) * 2 - 1
+        out["sigma"] = sig.to(torch.int8)
+    out["q"], out["k"], out["v"] = q.to(dt), k.to(dt), v.to(dt)
+    return out
+
+
+def sample_rows(w: Workload, inputs, n_target=2048, seed=12345):
+    """Deterministic sample of (seq, head, i) query rows for large problems.
+
+    Always includes rows 0, 127, 128, 255, 256 and the last row of every
+    (seq, head) (where they exist) plus, for varlen, the first and last row of
+    every sequence; the rest are uniform draws to reach ~n_target rows.
+    """
+    g = torch.Generator().manual_seed(seed)
+    if w.varlen:
+        lens = [int(x) for x in inputs["lengths"]]
+    else:
+        lens = [w.Sq] * w.B
+    rows = set()
+    for b, L in enumerate(lens):
+        for h in range(w.H):
+            for i in (0, 127, 128, 255, 256, L - 1):
+                if 0 <= i < L:
+                    rows.add((b, h, i))
+    pairs = [(b, h) for b in range(len(lens)) for h in range(w.H) if lens[b] > 0]
+    need = max(0, n_target - len(rows))
+    if need:
+        pi = torch.randint(0, len(pairs), (need,), generator=g).tolist()
+        u = torch.rand((need,), generator=g).tolist()
+        for p, x in zip(pi, u):
+            b, h = pairs[p]
+            rows.add((b, h, min(lens[b] - 1, int(x * lens[b]))))
+    return sorted(rows)
