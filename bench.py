@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward on GB300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl reference]
+
+A step is one attention forward (the whole hot path: one launch of the
+persistent kernel) over the workload's synthetic batch. The default workload
+is the bf16 B=4 H=16 Sq=Sk=8192 D=128 non-causal forward. Inputs are larger
+than L2 (384 MiB of Q/K/V), so no L2 flush runs between steps.
+
+``value`` is TFLOP/s (4*B*H*Sq*Sk*D, halved for causal) with inputs resident
+in HBM, timed with CUDA events on the launching stream; ``e2e`` is the same
+metric through the C ABI with the inputs copied from pinned host memory and
+the outputs copied back inside the timed region. ``roofline`` compares the
+kernel with the measured dense bf16 tensor-core peak; ``cpu_baseline`` times
+the fp64 oracle on the host cores on a bounded sample of the same workload.
+
+``--impl reference`` times the oracle itself as the reference arm (each step
+a bounded sample of the workload) and prints the same line with
+"impl": "reference".
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the
+workload (weak scaling: the forward shards over batch x heads with no data
+exchange); ``value`` = FLOPs of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of measured dense tensor-core ceiling"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def csrc_digest() -> str:
+    from exact_attention_forward_tiled_gb300 import build as fb
+    h = hashlib.sha256()
+    for d in (fb.CSRC, fb.INCLUDE):
+        for name in sorted(os.listdir(d)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(d, name), "rb") as f:
+                    h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = csrc_digest()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split())
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("csrc") == digest:
+                return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            self.out = ""
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(r[0] for r in rows)
+        loaded = [r for r in rows if r[0] >= 0.5 * top] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+def gemm_ceiling(torch, dev):
+    """Dense bf16 GEMM TFLOP/s measured in this run (cuBLAS through torch)."""
+    n = 8192
+    a = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    for _ in range(3):
+        torch.matmul(a, b)
+    best = 0.0
+    for _ in range(8):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        e1.synchronize()
+        best = max(best, 2 * n ** 3 / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    del a, b
+    return best
+
+
+def oracle_sample(w, inputs, seconds=10.0, max_rows=None):
+    """Time the fp64 oracle on query rows of one (sequence, head) of the
+    workload; rows are added until the sample takes about ``seconds``."""
+    from oracle import oracle as orc
+    import numpy as np
+    from exact_attention_forward_tiled_gb300 import accounting as A
+    if w.varlen:
+        cu = inputs["cu_seqlens_q"].cpu().tolist()
+        b = max(range(w.B), key=lambda i: cu[i + 1] - cu[i])
+        qs, qe = cu[b], cu[b + 1]
+        ks, ke = qs, qe
+    else:
+        qs, qe, ks, ke = 0, w.Sq, 0, w.Sk
+    q = orc._f64(inputs["q"][qs:qe, 0, :])
+    k = orc._f64(inputs["k"][ks:ke, 0, :])
+    v = orc._f64(inputs["v"][ks:ke, 0, :])
+    Lq, Lk = qe - qs, ke - ks
+    scale = w.D ** -0.5
+    rows = 16
+    rng = np.random.default_rng(0)
+    while True:
+        pos = np.sort(rng.choice(Lq, size=min(rows, Lq), replace=False))
+        t0 = time.perf_counter()
+        orc.attention_head(q[pos], pos, k, v, Lq, scale, w.causal)
+        dt = time.perf_counter() - t0
+        if dt >= seconds or len(pos) == Lq or (max_rows and rows >= max_rows):
+            break
+        rows = int(min(Lq, max(rows * 2, rows * seconds / max(dt, 1e-3) * 1.1)))
+        if max_rows:
+            rows = min(rows, max_rows)
+    pairs = orc.visible_pairs(pos, Lk, Lq, w.causal)
+    flops = 4.0 * pairs * w.D     # the same convention as the GPU metric, per visible pair
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{len(pos)} query rows of one (sequence, head) of {w.name} "
+                      f"(Lk={Lk}, D={w.D}, causal={w.causal}), fp64 C oracle with OpenMP, {dt:.2f} s",
+            "seconds": dt}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401
+    from exact_attention_forward_tiled_gb300 import workloads
+    from oracle import oracle as orc
+    orc.build()
+    w = workloads.WORKLOADS[args.workload]
+    inputs = workloads.make_inputs(w, device="cpu")
+    cal = oracle_sample(w, inputs, seconds=1.0)      # ~1 s per step
+    rows = max(1, int(cal["sample"].split()[0]))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(w, inputs, seconds=1e9, max_rows=rows)
+        if i >= args.warmup:
+            vals.append(r)
+    tot_s = sum(r["seconds"] for r in vals)
+    value = statistics.mean(r["value"] for r in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / len(vals),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
+                                            "D": w.D, "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's number of sequences (smaller profiling cases)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from exact_attention_forward_tiled_gb300 import accounting as A
+    from exact_attention_forward_tiled_gb300 import api, workloads
+    from exact_attention_forward_tiled_gb300 import build as fb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        fb.build()
+    if world > 1:
+        dist.barrier()
+    api.lib()
+
+    w = workloads.WORKLOADS[args.workload]
+    if args.batch is not None and not w.varlen:
+        from dataclasses import replace
+        w = replace(w, B=args.batch, name=f"{w.name}_B{args.batch}")
+    if w.dtype == "fp8":
+        raise SystemExit("the fp8 workload is benchmarked by its own entry points")
+    inputs = workloads.make_inputs(w, device=dev)
+    q, k, v = inputs["q"], inputs["k"], inputs["v"]
+    scale = w.D ** -0.5
+    o = torch.empty_like(q)
+    if w.varlen:
+        cu = inputs["cu_seqlens_q"]
+        lens = inputs["lengths"].tolist()
+        lse = torch.empty((w.H, q.shape[0]), device=dev, dtype=torch.float32)
+        Sq = Sk = inputs["max_seqlen"]
+        flops = A.attention_flops(w.H, w.D, lens, lens, w.causal)
+        extra = dict(cu_seqlens_q=cu, cu_seqlens_k=cu, total_q=q.shape[0], total_k=k.shape[0])
+    else:
+        lse = torch.empty((w.B, w.H, w.Sq), device=dev, dtype=torch.float32)
+        Sq, Sk = w.Sq, w.Sk
+        flops = A.attention_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
+        extra = {}
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qq=q, kk=k, vv=v, oo=o, ll=lse):
+        api.fa_fwd(qq, kk, vv, oo, ll, w.B, w.H, Sq, Sk, w.D, scale, w.causal, stream=stream, **extra)
+
+    for _ in range(args.warmup):
+        step()
+    api.fa_get_device_status(stream)
+    ceiling = gemm_ceiling(torch, dev)
+
+    def timed(fn, steps):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with ClockSampler(local) as clk:
+        total_ms = timed(step, args.steps)
+    api.fa_get_device_status(stream)
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the C ABI from pinned host buffers
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 50))
+    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
+    api.fa_get_device_status(stream)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    kern = "fa_fwd_kernel"
+    traffic = committed_traffic(kern, w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": Sq, "Sk": Sk, "D": w.D,
+                   "causal": w.causal, "varlen": w.varlen, "scale": scale,
+                   "l2": "inputs larger than L2 (no flush between steps)",
+                   "inputs": "Q,K,V iid N(0,1) fp32 -> %s, seed %d" % (w.dtype, w.seed)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense GEMM (burst), MEASURED_PEAKS.json",
+                     "kernel": kern},
+        "ceiling_in_run": {"bf16_gemm_tflops": ceiling, "frac": achieved / ceiling},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        cb = oracle_sample(w, {"q": q.cpu(), "k": k.cpu(), "v": v.cpu(),
+                               "cu_seqlens_q": inputs["cu_seqlens_q"]}, seconds=args.cpu_seconds)
+        cb.pop("seconds")
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

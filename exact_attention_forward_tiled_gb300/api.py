@@ -1,0 +1,133 @@
+"""Python binding of libfa.so: the C-ABI entry points under the same names.
+
+Argument marshalling only -- every step of the attention runs in the CUDA
+kernels behind the C ABI. Tensors are torch CUDA tensors (torch provides the
+device memory and the stream); nothing here computes attention, and there is
+no fallback: if the library is missing or the call fails, an exception says so.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "fa.h")
+
+FA_OK = 0
+FA_FP16, FA_BF16, FA_FP8_E4M3 = 0, 1, 2
+_DTYPE = {torch.float16: FA_FP16, torch.bfloat16: FA_BF16}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} ({status})")
+
+
+def header_functions():
+    """Names of the functions include/fa.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def lib():
+    """Load libfa.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.fa_fwd.restype = i
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, i, i, i, vp]
+        L.fa_get_device_status.restype = i
+        L.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i)]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_strerror.argtypes = [i]
+        L.fa_version.restype = i
+        L.fa_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def fa_version() -> int:
+    return lib().fa_version()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def fa_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q=None, cu_seqlens_k=None,
+           total_q=0, total_k=0, dtype=None, stream=None, check=True) -> int:
+    """Raw entry point: pointers from the tensors, sizes as given. Returns the
+    status; raises FAError when ``check`` and the status is not FA_OK."""
+    if dtype is None:
+        dtype = _DTYPE[q.dtype]
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(Sq), int(Sk),
+                      int(D), float(scale), int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                      int(total_q), int(total_k), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return st
+
+
+def fa_get_device_status(stream=None, check=True):
+    raw = ctypes.c_int(0)
+    st = lib().fa_get_device_status(_stream(stream), ctypes.byref(raw))
+    if check and st != FA_OK:
+        raise FAError(st, f"device status word 0x{raw.value:x}")
+    return st, raw.value
+
+
+def attention_forward(q, k, v, *, causal=False, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
+                      max_seqlen_q=None, max_seqlen_k=None, batch=None, out=None, lse=None, stream=None):
+    """Allocate O and LSE and call ``fa_fwd``.
+
+    Fixed length: q ``[B*Sq, H, D]`` (or ``[B, Sq, H, D]``), k/v likewise; give
+    ``batch`` when passing the flattened form. Varlen: ``cu_seqlens_*`` int32
+    CUDA tensors and ``max_seqlen_*``. Returns (O, LSE) with LSE fp32
+    ``[B, H, Sq]`` (fixed) or ``[H, total_q]`` (varlen).
+    """
+    if q.dim() == 4:
+        B, Sq, H, D = q.shape
+        Sk = k.shape[1]
+        q, k, v = q.reshape(B * Sq, H, D), k.reshape(B * Sk, H, D), v.reshape(B * Sk, H, D)
+    else:
+        H, D = q.shape[1], q.shape[2]
+        if cu_seqlens_q is None:
+            B = batch
+            Sq, Sk = q.shape[0] // B, k.shape[0] // B
+        else:
+            B = cu_seqlens_q.numel() - 1
+            Sq, Sk = max_seqlen_q, max_seqlen_k
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        shape = (H, q.shape[0]) if cu_seqlens_q is not None else (B, H, Sq)
+        lse = torch.empty(shape, device=q.device, dtype=torch.float32)
+    fa_fwd(q, k, v, out, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q, cu_seqlens_k,
+           q.shape[0], k.shape[0], stream=stream)
+    return out, lse

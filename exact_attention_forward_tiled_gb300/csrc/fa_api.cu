@@ -1,0 +1,211 @@
+// C-ABI front end of libfa.so: argument checks, TMA tensor maps, kernel
+// selection and launch, device status word. See include/fa.h for the contract.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+// Device status word (one per device that loads the library): kernels OR in
+// fa::kDev* codes; fa_get_device_status() reads and clears it.
+__device__ int g_fa_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+int current_device(DevInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return FA_ERR_NO_DEVICE;  // kernels are built for sm_103a
+    void* sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_fa_status) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    d.status = static_cast<int*>(sym);
+    d.sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D map over a [rows, cols] row-major matrix, boxes of box_rows x box_cols,
+// 128-byte swizzle (the layout the tcgen05 descriptors expect), zero fill
+// outside the matrix.
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t cols,
+             uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[2] = {cols, rows < 1 ? 1 : rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return (1 << 16) | 0; }
+
+const char* fa_strerror(int s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out; outputs incomplete";
+    case FA_ERR_DEVICE_SEQLENS: return "cu_seqlens entry out of bounds; sequence skipped";
+    case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+           int Sk, int D, float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+           int total_q, int total_k, int dtype, void* stream) {
+  // ---- host-side argument checks (no device access)
+  if (dtype == FA_FP8_E4M3) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
+  if (varlen && (total_q < 0 || total_k < 0)) return FA_ERR_INVALID_ARG;
+  const int64_t Tq = varlen ? total_q : (int64_t)B * Sq;
+  const int64_t Tk = varlen ? total_k : (int64_t)B * Sk;
+  if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)H * D * 2 > (int64_t)1 << 38) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0 || Sq == 0) return FA_OK;  // nothing to compute
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_ALIGNMENT;
+  const int rows = fa::cta_rows(D);
+  const int64_t n_qblk = ((int64_t)Sq + rows - 1) / rows;
+  const int64_t ntiles = (int64_t)B * H * n_qblk;
+  if (ntiles > INT32_MAX || (int64_t)B * H * Sq > ((int64_t)1 << 40)) return FA_ERR_INVALID_ARG;
+
+  // ---- device
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const CUtensorMapDataType dt = dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t cols = (uint64_t)H * D;
+  if ((st = make_map(&L.tq, q, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tk, k, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tv, v, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
+  L.p.o = o;
+  L.p.lse = lse;
+  L.p.cu_q = cu_seqlens_q;
+  L.p.cu_k = cu_seqlens_k;
+  L.p.B = B;
+  L.p.H = H;
+  L.p.Sq = Sq;
+  L.p.Sk = Sk;
+  L.p.total_q = (int)Tq;
+  L.p.total_k = (int)Tk;
+  L.p.n_qblk = (int)n_qblk;
+  L.p.ntiles = (int)ntiles;
+  L.p.c = (float)((double)scale * 1.4426950408889634);
+  L.p.status = dev->status;
+  L.p.tile_counter = nullptr;
+  L.D = D;
+  L.fp16 = dtype == FA_FP16;
+  L.causal = causal != 0;
+  L.num_sms = dev->sms;
+  L.stream = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  switch (D) {
+    case 64: e = fa::launch_fwd_d64(L); break;
+    case 128: e = fa::launch_fwd_d128(L); break;
+    default: e = fa::launch_fwd_d256(L); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_get_device_status(void* stream, int* raw) {
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  int word = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  if (raw) *raw = word;
+  if (word & fa::kDevTimeout) return FA_ERR_DEVICE_TIMEOUT;
+  if (word & fa::kDevBadSeqlens) return FA_ERR_DEVICE_SEQLENS;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,571 @@
+// Exact tiled attention forward for sm_103a (GB300).
+//
+// O = softmax(scale * Q K^T [+ causal mask]) V and LSE = ln sum exp(scale * Q K^T),
+// computed tile by tile with the online-softmax running max / sum recurrence
+// ("Flash Attention 3 principles (guijiagi)", sections 2.1-2.2 and 3.1: Q is
+// split into 128-row tiles that each CTA owns end to end, K/V stream through
+// on-chip memory in 128-row tiles, only O and LSE are written back).
+//
+// One persistent CTA per SM runs a sequence of work tiles. Each work tile is
+// QT query tiles of 128 rows of one (sequence, head) -- QT = 2 for D <= 128,
+// 1 for D = 256 -- and the CTA's warps have fixed roles:
+//
+//   softmax warpgroups (4 warps per query tile, thread r owns row r)
+//       tcgen05.ld the fp32 score row from tensor memory, mask, row max,
+//       lazy rescale of O (only when the row max grows by more than TAU in
+//       log2 units), P = exp2(S * scale * log2 e - m), row sum, P -> 16-bit,
+//       tcgen05.st P back into tensor memory over its scores; at the end of
+//       the work tile O / l and LSE are written to global memory.
+//   MMA warp (one thread)
+//       tcgen05.mma kind::f16: S_t = Q_t K_j^T (both operands in shared
+//       memory) and O_t += P_t V_j (P from tensor memory, V from shared
+//       memory), accumulators in tensor memory; tcgen05.commit signals
+//       mbarriers. For QT = 2 the issue order QK0_j, PV1_{j-1}, QK1_j, PV0_j
+//       keeps the tensor core busy while the two softmax warpgroups take
+//       turns (the ping-pong idea of the FlashAttention-3 wiki, technique 1,
+//       done with two tensor-memory score buffers instead of two register
+//       files).
+//   load warp (one thread)
+//       TMA loads of the Q tiles and of K_j, V_j into a ring of shared-memory
+//       slots guarded by full / empty mbarriers (producer / consumer of the
+//       wiki's technique 1; multi-stage K/V pipeline of technique 2).
+//
+// Every wait on an mbarrier is bounded: after WAIT_LIMIT_NS the waiting role
+// records a timeout in the device status word, raises an abort flag that the
+// other roles see, and all roles leave; tensor memory is freed on the way out.
+#pragma once
+
+#include <cstdint>
+#include <math_constants.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr float kTau = 8.0f;                      // lazy-rescale threshold (log2 units)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D_, int QT_, int STAGES_>
+struct FwdCfg {
+  static constexpr int D = D_;
+  static constexpr int QT = QT_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int kRows = 128 * QT;          // query rows per work tile
+  static constexpr int kBoxes = D / 64;           // 64-element (128-byte) column boxes
+  static constexpr int kBoxBytes = 128 * 128;     // one box: 128 rows x 128 bytes
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kSoftmaxWarps = 4 * QT;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kLoadWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+  static constexpr int kTmemCols = 512;
+  // tensor-memory columns: score buffers S0, S1; accumulators O0 (, O1)
+  __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return b ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t col_o(uint32_t t) { return 256u + t * D; }
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = QT * kTileBytes;
+  static constexpr int kOffBar = kOffKV + STAGES * kTileBytes;
+  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+  // o_full[2], pv_done, mma_done
+  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + STAGES,
+                       kBarSFull = 2 + 2 * STAGES, kBarPFull = kBarSFull + 2,
+                       kBarOFull = kBarPFull + 2, kBarPVDone = kBarOFull + 2,
+                       kBarMmaDone = kBarPVDone + 1, kNumBars = kBarMmaDone + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+
+  static_assert(D == 64 || D == 128 || D == 256, "head dimension");
+  static_assert(QT == 1 || 2 * 128 + QT * D <= kTmemCols, "tensor memory budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Work tile: CTA query block of one (sequence, head).
+struct TileInfo {
+  int b, h;
+  int q0;        // first query row of the block within its sequence
+  int Lq, Lk;    // sequence lengths
+  int qtok, ktok;  // token index of row 0 of the sequence in Q/O and in K/V
+  int n_kv;      // key blocks of 128 to visit
+  bool live;     // false: the block starts beyond the sequence
+};
+
+// Heads are the outer loop so that the CTAs running at the same time share
+// their K/V through L2; under the causal mask the blocks of a head are
+// visited from the most expensive (last rows) to the cheapest.
+template <int ROWS, bool CAUSAL>
+__device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
+  TileInfo t;
+  const int bh = w / p.n_qblk;
+  const int j = w - bh * p.n_qblk;
+  const int qblk = CAUSAL ? (p.n_qblk - 1 - j) : j;
+  t.b = bh / p.H;
+  t.h = bh - t.b * p.H;
+  if (p.cu_q != nullptr) {
+    const int qs = __ldg(p.cu_q + t.b), qe = __ldg(p.cu_q + t.b + 1);
+    const int ks = __ldg(p.cu_k + t.b), ke = __ldg(p.cu_k + t.b + 1);
+    t.qtok = qs;
+    t.ktok = ks;
+    t.Lq = qe - qs;
+    t.Lk = ke - ks;
+    // a sequence that breaks the declared bounds is skipped (and reported)
+    if (qs < 0 || qe < qs || qe > p.total_q || ks < 0 || ke < ks || ke > p.total_k ||
+        t.Lq > p.Sq || t.Lk > p.Sk) {
+      t.Lq = 0;
+      t.Lk = 0;
+      if (qblk == 0) atomicOr(p.status, kDevBadSeqlens);
+    }
+  } else {
+    t.qtok = t.b * p.Sq;
+    t.ktok = t.b * p.Sk;
+    t.Lq = p.Sq;
+    t.Lk = p.Sk;
+  }
+  t.q0 = qblk * ROWS;
+  t.live = t.q0 < t.Lq;
+  int n = 0;
+  if (t.live) {
+    const int last = min(t.q0 + ROWS, t.Lq) - 1;
+    int lim = t.Lk;
+    if (CAUSAL) lim = min(lim, last + t.Lk - t.Lq + 1);
+    n = lim > 0 ? (lim + 127) / 128 : 0;
+  }
+  t.n_kv = n;
+  return t;
+}
+
+// Bounded mbarrier waits shared by all roles of a CTA.
+struct Waiter {
+  volatile int* abort_flag;
+  int* status;
+
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int where) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((n & 63u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(status, kDevTimeout | where);
+          return false;
+        }
+      }
+    }
+  }
+  // Whole-warp wait: every lane waits; the warp proceeds only if all did.
+  __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, int where) const {
+    const bool ok = wait(bar, parity, where);
+    return __all_sync(0xffffffffu, ok);
+  }
+  // Drain wait used on the way out: bounded, ignores the abort flag.
+  __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ load warp
+template <class C, bool CAUSAL>
+__device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                          const FwdParams& p, uint32_t sbase, const Waiter& wt) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t kvc = 0, tcount = 0;
+  bool ok = true;
+
+  auto load_tile = [&](const CUtensorMap* m, int h, int row, uint32_t dst, uint32_t b) {
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxes; ++bx)
+      ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * 64, row, b);
+  };
+  auto load_kv = [&](const CUtensorMap* m, int h, int row) -> bool {
+    const int s = kvc % C::STAGES;
+    const uint32_t ph = (kvc / C::STAGES) & 1u;
+    if (!wt.wait(bar(C::kBarKVEmpty + s), ph ^ 1u, 2)) return false;
+    ptx::mbar_arrive_expect_tx(bar(C::kBarKVFull + s), C::kTileBytes);
+    load_tile(m, h, row, sbase + C::kOffKV + s * C::kTileBytes, bar(C::kBarKVFull + s));
+    ++kvc;
+    return true;
+  };
+
+  for (int w = blockIdx.x; ok && w < p.ntiles; w += gridDim.x) {
+    const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
+    if (ti.n_kv == 0) continue;
+    if (!wt.wait(bar(C::kBarQEmpty), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
+    ptx::mbar_arrive_expect_tx(bar(C::kBarQFull), C::QT * C::kTileBytes);
+#pragma unroll
+    for (int t = 0; t < C::QT; ++t)
+      load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
+                bar(C::kBarQFull));
+    ++tcount;
+    const int n = ti.n_kv;
+    if (C::QT == 2) {
+      // consumption order of the MMA warp: K0, V0, K1, V1, ...
+      for (int i = 0; ok && i < n; ++i) {
+        ok = load_kv(tk, ti.h, ti.ktok + 128 * i) && load_kv(tv, ti.h, ti.ktok + 128 * i);
+      }
+    } else {
+      // consumption order: K0, K1, V0, K2, V1, ..., V_{n-1}
+      ok = load_kv(tk, ti.h, ti.ktok);
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n) ok = load_kv(tk, ti.h, ti.ktok + 128 * (i + 1));
+        if (ok) ok = load_kv(tv, ti.h, ti.ktok + 128 * i);
+      }
+    }
+  }
+  if (*wt.abort_flag) {
+    // let the copies still in flight land before the CTA's memory goes away
+    const uint32_t first = kvc > (uint32_t)C::STAGES ? kvc - C::STAGES : 0u;
+    for (uint32_t c = first; c < kvc; ++c)
+      wt.drain(bar(C::kBarKVFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u);
+    if (tcount > 0) wt.drain(bar(C::kBarQFull), (tcount - 1) & 1u);
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp
+template <class C, bool FP16, bool CAUSAL>
+__device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  constexpr uint32_t fmt = FP16 ? 0u : 1u;
+  constexpr uint32_t idesc_qk = ptx::make_idesc(fmt, false, 128, 128);
+  constexpr uint32_t idesc_pv = ptx::make_idesc(fmt, true, 128, C::D);
+  const uint32_t sq = sbase + C::kOffQ;
+  auto slot_addr = [&](uint32_t c) { return sbase + C::kOffKV + (c % C::STAGES) * C::kTileBytes; };
+  auto slot = [&](uint32_t c) { return (int)(c % C::STAGES); };
+
+  // S[s_col] = Q_t K^T : D/16 steps of K = 16 along the head dimension
+  auto qk = [&](uint32_t s_col, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+      ptx::mma_f16_ss(tmem + s_col, ptx::smem_desc_sw128(q_addr + off, 16, 1024),
+                      ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
+    }
+  };
+  // O[o_col] (+)= P[p_col] V : 8 steps of K = 16 keys; P packs 2 keys per column
+  auto pv = [&](uint32_t o_col, uint32_t p_col, uint32_t v_addr, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      ptx::mma_f16_ts(tmem + o_col, tmem + p_col + kk * 8,
+                      ptx::smem_desc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
+                      (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+  auto kv_ready = [&](uint32_t c) {
+    const bool r = wt.wait(bar(C::kBarKVFull + slot(c)), (c / C::STAGES) & 1u, 4);
+    ptx::tc_fence_after();
+    return r;
+  };
+
+  uint32_t kvc = 0, it = 0, tcount = 0;
+  bool ok = true;
+  for (int w = blockIdx.x; ok && w < p.ntiles; w += gridDim.x) {
+    const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
+    if (ti.n_kv == 0) continue;
+    if (!wt.wait(bar(C::kBarQFull), tcount & 1u, 3)) { ok = false; break; }
+    ++tcount;
+    ptx::tc_fence_after();
+    const int n = ti.n_kv;
+    if (C::QT == 2) {
+      if (!(ok = kv_ready(kvc))) break;
+      qk(C::col_s(0), sq, slot_addr(kvc));
+      ptx::mma_commit(bar(C::kBarSFull + 0));
+      for (int i = 0; i < n; ++i) {
+        const uint32_t ck = kvc + 2 * i, cv = ck + 1;
+        if (i > 0) {
+          if (!(ok = wt.wait(bar(C::kBarPFull + 1), (it + i - 1) & 1u, 5))) break;
+          ptx::tc_fence_after();
+          pv(C::col_o(1), C::col_s(1), slot_addr(cv - 2), i - 1 > 0);
+          ptx::mma_commit(bar(C::kBarKVEmpty + slot(cv - 2)));
+        }
+        qk(C::col_s(1), sq + C::kTileBytes, slot_addr(ck));
+        ptx::mma_commit(bar(C::kBarSFull + 1));
+        ptx::mma_commit(bar(C::kBarKVEmpty + slot(ck)));
+        if (i == n - 1) ptx::mma_commit(bar(C::kBarQEmpty));
+        if (!(ok = kv_ready(cv))) break;
+        if (!(ok = wt.wait(bar(C::kBarPFull + 0), (it + i) & 1u, 5))) break;
+        ptx::tc_fence_after();
+        pv(C::col_o(0), C::col_s(0), slot_addr(cv), i > 0);
+        if (i == n - 1) ptx::mma_commit(bar(C::kBarOFull + 0));
+        if (i + 1 < n) {
+          if (!(ok = kv_ready(ck + 2))) break;
+          qk(C::col_s(0), sq, slot_addr(ck + 2));
+          ptx::mma_commit(bar(C::kBarSFull + 0));
+        }
+      }
+      if (!ok) break;
+      if (!(ok = wt.wait(bar(C::kBarPFull + 1), (it + n - 1) & 1u, 5))) break;
+      ptx::tc_fence_after();
+      const uint32_t cl = kvc + 2 * n - 1;
+      pv(C::col_o(1), C::col_s(1), slot_addr(cl), n - 1 > 0);
+      ptx::mma_commit(bar(C::kBarKVEmpty + slot(cl)));
+      ptx::mma_commit(bar(C::kBarOFull + 1));
+      kvc += 2 * n;
+      it += n;
+    } else {
+      if (!(ok = kv_ready(kvc))) break;
+      qk(C::col_s(it & 1u), sq, slot_addr(kvc));
+      ptx::mma_commit(bar(C::kBarSFull + (int)(it & 1u)));
+      ptx::mma_commit(bar(C::kBarKVEmpty + slot(kvc)));
+      ++kvc;
+      if (n == 1) ptx::mma_commit(bar(C::kBarQEmpty));
+      for (int i = 0; i < n; ++i) {
+        const uint32_t iti = it + i;
+        if (i + 1 < n) {
+          if (!(ok = kv_ready(kvc))) break;
+          qk(C::col_s((iti + 1) & 1u), sq, slot_addr(kvc));
+          ptx::mma_commit(bar(C::kBarSFull + (int)((iti + 1) & 1u)));
+          ptx::mma_commit(bar(C::kBarKVEmpty + slot(kvc)));
+          ++kvc;
+          if (i + 1 == n - 1) ptx::mma_commit(bar(C::kBarQEmpty));
+        }
+        if (!(ok = kv_ready(kvc))) break;
+        if (!(ok = wt.wait(bar(C::kBarPFull + (int)(iti & 1u)), (iti >> 1) & 1u, 5))) break;
+        ptx::tc_fence_after();
+        pv(C::col_o(0), C::col_s(iti & 1u), slot_addr(kvc), i > 0);
+        ptx::mma_commit(bar(C::kBarKVEmpty + slot(kvc)));
+        ptx::mma_commit(bar(C::kBarPVDone));
+        ++kvc;
+        if (i == n - 1) ptx::mma_commit(bar(C::kBarOFull + 0));
+      }
+      it += n;
+    }
+  }
+  // all issued MMAs complete before tensor memory can be released
+  ptx::mma_commit(bar(C::kBarMmaDone));
+  wt.drain(bar(C::kBarMmaDone), 0);
+}
+
+// ------------------------------------------------------------------ softmax warpgroups
+template <bool FP16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return FP16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
+}
+
+template <class C, bool FP16, bool CAUSAL>
+__device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
+                             int t, int quarter) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  const int lane = threadIdx.x & 31;
+  const int r = quarter * 32 + lane;                         // row within the 128-row tile
+  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
+  const float c = p.c;
+  const float NEG_INF = -CUDART_INF_F;
+
+  uint32_t it = 0, tcount = 0;
+  for (int w = blockIdx.x; w < p.ntiles; w += gridDim.x) {
+    const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
+    if (!ti.live) continue;
+    const int row = ti.q0 + 128 * t + r;
+    const bool row_ok = row < ti.Lq;
+    const int64_t tok = (int64_t)ti.qtok + row;
+    uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + ti.h) * C::D;
+    float* lse_ptr = p.cu_q != nullptr
+                         ? p.lse + (int64_t)ti.h * p.total_q + tok
+                         : p.lse + ((int64_t)ti.b * p.H + ti.h) * p.Sq + row;
+    if (ti.n_kv == 0) {
+      // no visible key for any row of this block: O = 0, LSE = -inf
+      if (row_ok) {
+        for (int d = 0; d < C::D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        *lse_ptr = NEG_INF;
+      }
+      continue;
+    }
+    const int key_lim = CAUSAL ? min(ti.Lk, row + ti.Lk - ti.Lq + 1) : ti.Lk;
+    float m_ref = NEG_INF, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < ti.n_kv; ++i, ++it) {
+      const int buf = C::QT == 2 ? t : (int)(it & 1u);
+      const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
+      if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;
+      ptx::tc_fence_after();
+      const uint32_t s_addr = tl + C::col_s(buf);
+      float s[128];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          ptx::tmem_ld32(s_addr + 32 * ch, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[32 * ch + j] = __uint_as_float(v[j]);
+        }
+      }
+      const int lim_local = key_lim - 128 * i;
+      const bool masked = lim_local < 128;   // keys j >= lim_local are not visible
+      if (masked) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) s[j] = j < lim_local ? s[j] : NEG_INF;
+      }
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx[a] = s[a];
+#pragma unroll
+      for (int j = 8; j < 128; j += 8)
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(mx[a], s[j + a]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_tile = mt == NEG_INF ? NEG_INF : mt * c;  // scaled log2 units (c >= 0)
+      if (i == 0) {
+        m_ref = m_tile;
+      } else {
+        const bool need = m_tile > m_ref + kTau;
+        if (__any_sync(0xffffffffu, need)) {
+          if (C::QT == 1) {
+            // the previous PV must have landed in O before it is rescaled
+            if (!(ok = wt.wait_warp(bar(C::kBarPVDone), (it - 1) & 1u, 8))) break;
+            ptx::tc_fence_after();
+          }
+          const float alpha = need ? ptx::ex2(m_ref - m_tile) : 1.f;
+          if (need) {
+            m_ref = m_tile;
+            l *= alpha;
+          }
+          const uint32_t o_addr = tl + C::col_o(t);
+#pragma unroll 1
+          for (int ch = 0; ch < C::D / 32; ++ch) {
+            uint32_t v[32];
+            ptx::tmem_ld32(o_addr + 32 * ch, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            ptx::tmem_st32(o_addr + 32 * ch, v);
+          }
+          ptx::tmem_wait_st();
+        }
+      }
+      const float mu = m_ref == NEG_INF ? 0.f : m_ref;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) s[j] = ptx::ex2(fmaf(s[j], c, -mu));
+      if (masked) {
+        // zero the invisible keys after the exponent: with c = 0 their
+        // -inf * c would be NaN
+#pragma unroll
+        for (int j = 0; j < 128; ++j) s[j] = j < lim_local ? s[j] : 0.f;
+      }
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 128; ++j) ls[j & 3] += s[j];
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack2<FP16>(s[2 * j], s[2 * j + 1]);
+        ptx::tmem_st32(s_addr, pk);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack2<FP16>(s[64 + 2 * j], s[64 + 2 * j + 1]);
+        ptx::tmem_st32(s_addr + 32, pk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + buf));
+    }
+    if (!ok) return;
+    // epilogue: O / l, LSE
+    if (!wt.wait_warp(bar(C::kBarOFull + (C::QT == 2 ? t : 0)), tcount & 1u, 7)) return;
+    ++tcount;
+    ptx::tc_fence_after();
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const uint32_t o_addr = tl + C::col_o(C::QT == 2 ? t : 0);
+#pragma unroll 1
+    for (int ch = 0; ch < C::D / 32; ++ch) {
+      uint32_t v[32];
+      ptx::tmem_ld32(o_addr + 32 * ch, v);
+      ptx::tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack2<FP16>(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+    if (row_ok) *lse_ptr = l > 0.f ? (m_ref + ptx::lg2(l)) * kLn2 : NEG_INF;
+    // the next work tile's PV may overwrite O only after these reads
+    ptx::tc_fence_before();
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, int QT, int STAGES, bool FP16, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D, QT, STAGES>::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = FwdCfg<D, QT, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  if (threadIdx.x == 0) {
+    const uint32_t bars = sbase + C::kOffBar;
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const bool is_pfull = i == C::kBarPFull || i == C::kBarPFull + 1;
+      ptx::mbar_init(bars + 8u * i, is_pfull ? 4u : 1u);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    ptx::prefetch_tmap(&tq);
+    ptx::prefetch_tmap(&tk);
+    ptx::prefetch_tmap(&tv);
+  }
+  if (warp == C::kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const Waiter wt{abort_flag, p.status};
+
+  if (warp == C::kLoadWarp) {
+    if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt);
+  } else if (warp == C::kMmaWarp) {
+    if (lane == 0) mma_role<C, FP16, CAUSAL>(p, sbase, tmem, wt);
+  } else {
+    softmax_role<C, FP16, CAUSAL>(p, sbase, tmem, wt, warp >> 2, warp & 3);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int QT, int STAGES>
+cudaError_t launch_fwd_impl(const FwdLaunch& L) {
+  using C = FwdCfg<D, QT, STAGES>;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams);
+  if (L.fp16)
+    kern = L.causal ? fa_fwd_kernel<D, QT, STAGES, true, true> : fa_fwd_kernel<D, QT, STAGES, true, false>;
+  else
+    kern = L.causal ? fa_fwd_kernel<D, QT, STAGES, false, true> : fa_fwd_kernel<D, QT, STAGES, false, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int grid = L.p.ntiles < L.num_sms ? L.p.ntiles : L.num_sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tq, L.tk, L.tv, L.p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,99 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact, IO-aware tiled attention forward on GB300
+ * (sm_103a), written for tcgen05 tensor cores, tensor memory and TMA.
+ *
+ * The operation ("Flash Attention 3 principles (guijiagi)", section 1.2 for
+ * standard attention, section 2.2 for the online-softmax recurrence the kernel
+ * uses, section 5.2 for the varlen call with `causal` and `softmax_scale`):
+ *
+ *   for every sequence b, head h and query row i of that sequence,
+ *     s_ij  = scale * sum_d Q[i,h,d] K[j,h,d]        for visible keys j
+ *     O[i,h,:] = sum_j exp(s_ij - m_i) V[j,h,:] / sum_j exp(s_ij - m_i)
+ *     LSE[i,h] = m_i + ln sum_j exp(s_ij - m_i)        (natural log)
+ *   with m_i the row max; visible keys are j < Lk, and with `causal` only
+ *   j <= i + Lk - Lq (mask aligned to the bottom-right corner; for Lq = Lk
+ *   this is j <= i). A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers on the current CUDA device.
+ *     The caller owns every buffer; the library keeps none of them.
+ *   - Q/K/V/O layout: contiguous [tokens, H, D] (row-major, D fastest), i.e.
+ *     (B, S, H, D) for fixed length (tokens = B*S, batch-major) or packed
+ *     sequences for varlen. Base pointers must be 16-byte aligned.
+ *   - D (head dimension) is 64, 128 or 256.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous on it; argument errors are reported synchronously
+ *     by the return value, errors found on the device by
+ *     fa_get_device_status().
+ *   - Return value: FA_OK (0) or a negative FA_ERR_* code (fa_strerror()).
+ *   - The library allocates no memory per call. Its only device state is one
+ *     status word per device (a static __device__ variable).
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID_ARG -1     /* a size, pointer or flag is out of range   */
+#define FA_ERR_UNSUPPORTED -2     /* valid request this build does not support */
+#define FA_ERR_ALIGNMENT -3       /* a pointer is not 16-byte aligned          */
+#define FA_ERR_CUDA -4            /* a CUDA runtime / driver call failed       */
+#define FA_ERR_DEVICE_TIMEOUT -5  /* a kernel wait gave up (see status)        */
+#define FA_ERR_DEVICE_SEQLENS -6  /* a cu_seqlens entry broke its bounds       */
+#define FA_ERR_NO_DEVICE -7       /* no sm_100-family device is current        */
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
+
+/*
+ * fa_fwd -- attention forward for 16-bit inputs (FA_FP16 or FA_BF16).
+ *
+ *   q            [Tq, H, D] 16-bit, Tq = B*Sq (fixed) or total_q (varlen)
+ *   k, v         [Tk, H, D] same type, Tk = B*Sk or total_k
+ *   o            [Tq, H, D] output, same type as q (written)
+ *   lse          fp32 output: [B, H, Sq] (fixed) or [H, total_q] (varlen)
+ *   B            number of sequences (fixed: batch size)
+ *   H, D         heads, head dimension
+ *   Sq, Sk       fixed: query / key length of every sequence;
+ *                varlen: upper bounds of the lengths (max_seqlen_q / _k)
+ *   scale        softmax scale, finite and >= 0 (1/sqrt(D) in the pages)
+ *   causal       0 or 1
+ *   cu_seqlens_q, cu_seqlens_k
+ *                NULL for fixed length; for varlen both are device int32
+ *                arrays of B+1 nondecreasing prefix sums starting at 0
+ *   total_q, total_k
+ *                varlen only: rows of q/o and of k/v (cu_seqlens[B] may not
+ *                exceed them); ignored for fixed length
+ *   dtype        FA_FP16 or FA_BF16 (FA_FP8_E4M3 -> FA_ERR_UNSUPPORTED; the
+ *                8-bit path has its own entry points)
+ *
+ * A varlen sequence whose lengths break the bounds is skipped on the device
+ * and reported as FA_ERR_DEVICE_SEQLENS by fa_get_device_status().
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int Sq, int Sk, int D, float scale, int causal,
+           const int* cu_seqlens_q, const int* cu_seqlens_k, int total_q, int total_k,
+           int dtype, void* stream);
+
+/*
+ * fa_get_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word. Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a
+ * kernel's bounded wait expired; the kernel left early and its outputs are
+ * incomplete), FA_ERR_DEVICE_SEQLENS, or FA_ERR_CUDA. `raw` (may be NULL)
+ * receives the raw word for diagnosis.
+ */
+int fa_get_device_status(void* stream, int* raw);
+
+/* Human-readable text of a status code (static storage). */
+const char* fa_strerror(int status);
+
+/* ABI version of this header, (major << 16) | minor. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */
