@@ -150,41 +150,42 @@ def gemm_ceiling(torch, dev):
 
 
 def oracle_sample(w, inputs, seconds=10.0, max_rows=None):
-    """Time the fp64 oracle on query rows of one (sequence, head) of the
-    workload; rows are added until the sample takes about ``seconds``."""
+    """Time the fp64 oracle on a bounded sample of the workload: whole
+    (sequence, head) pairs in order until the sample has taken ``seconds``
+    (or, with ``max_rows``, that many rows of the first pair)."""
     from oracle import oracle as orc
     import numpy as np
-    from exact_attention_forward_tiled_gb300 import accounting as A
     if w.varlen:
         cu = inputs["cu_seqlens_q"].cpu().tolist()
-        b = max(range(w.B), key=lambda i: cu[i + 1] - cu[i])
-        qs, qe = cu[b], cu[b + 1]
-        ks, ke = qs, qe
+        bounds = [(cu[b], cu[b + 1]) for b in range(w.B)]
     else:
-        qs, qe, ks, ke = 0, w.Sq, 0, w.Sk
-    q = orc._f64(inputs["q"][qs:qe, 0, :])
-    k = orc._f64(inputs["k"][ks:ke, 0, :])
-    v = orc._f64(inputs["v"][ks:ke, 0, :])
-    Lq, Lk = qe - qs, ke - ks
+        bounds = [(b * w.Sq, (b + 1) * w.Sq) for b in range(w.B)]
     scale = w.D ** -0.5
-    rows = 16
-    rng = np.random.default_rng(0)
-    while True:
-        pos = np.sort(rng.choice(Lq, size=min(rows, Lq), replace=False))
-        t0 = time.perf_counter()
-        orc.attention_head(q[pos], pos, k, v, Lq, scale, w.causal)
-        dt = time.perf_counter() - t0
-        if dt >= seconds or len(pos) == Lq or (max_rows and rows >= max_rows):
+    spent, pairs, rows, heads = 0.0, 0, 0, 0
+    for b, (s0, s1) in enumerate(bounds):
+        for h in range(w.H):
+            L = s1 - s0
+            if L == 0:
+                continue
+            q = orc._f64(inputs["q"][s0:s1, h, :])
+            k = orc._f64(inputs["k"][s0:s1, h, :])
+            v = orc._f64(inputs["v"][s0:s1, h, :])
+            pos = np.arange(L) if max_rows is None else np.arange(min(L, max_rows))
+            t0 = time.perf_counter()
+            orc.attention_head(q[pos], pos, k, v, L, scale, w.causal)
+            spent += time.perf_counter() - t0
+            pairs += orc.visible_pairs(pos, L, L, w.causal)
+            rows += len(pos)
+            heads += 1
+            if spent >= seconds or max_rows is not None:
+                break
+        if spent >= seconds or max_rows is not None:
             break
-        rows = int(min(Lq, max(rows * 2, rows * seconds / max(dt, 1e-3) * 1.1)))
-        if max_rows:
-            rows = min(rows, max_rows)
-    pairs = orc.visible_pairs(pos, Lk, Lq, w.causal)
     flops = 4.0 * pairs * w.D     # the same convention as the GPU metric, per visible pair
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"{len(pos)} query rows of one (sequence, head) of {w.name} "
-                      f"(Lk={Lk}, D={w.D}, causal={w.causal}), fp64 C oracle with OpenMP, {dt:.2f} s",
-            "seconds": dt}
+    return {"value": flops / spent / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{rows} query rows ({heads} whole (sequence, head) pairs) of {w.name}, "
+                      f"fp64 C oracle with OpenMP, {spent:.2f} s",
+            "seconds": spent, "rows": rows}
 
 
 def run_reference(args):
@@ -198,8 +199,9 @@ def run_reference(args):
     orc.build()
     w = workloads.WORKLOADS[args.workload]
     inputs = workloads.make_inputs(w, device="cpu")
-    cal = oracle_sample(w, inputs, seconds=1.0)      # ~1 s per step
-    rows = max(1, int(cal["sample"].split()[0]))
+    # one step = the rows of the first (sequence, head) that take ~1 s
+    probe = oracle_sample(w, inputs, seconds=0.0, max_rows=256)
+    rows = max(16, int(256 * 1.0 / max(probe["seconds"], 1e-3)))
     vals = []
     for i in range(args.warmup + args.steps):
         r = oracle_sample(w, inputs, seconds=1e9, max_rows=rows)
