@@ -262,12 +262,12 @@ def main(argv=None):
     if args.batch is not None and not w.varlen:
         from dataclasses import replace
         w = replace(w, B=args.batch, name=f"{w.name}_B{args.batch}")
-    if w.dtype == "fp8":
-        raise SystemExit("the fp8 workload is benchmarked by its own entry points")
+    fp8 = w.dtype == "fp8"
     inputs = workloads.make_inputs(w, device=dev)
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
     scale = w.D ** -0.5
-    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, device=dev)
     if w.varlen:
         cu = inputs["cu_seqlens_q"]
         lens = inputs["lengths"].tolist()
@@ -280,24 +280,47 @@ def main(argv=None):
         Sq, Sk = w.Sq, w.Sk
         flops = A.attention_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
         extra = {}
-    stream = torch.cuda.current_stream(dev)
 
-    def step(qq=q, kk=k, vv=v, oo=o, ll=lse):
-        api.fa_fwd(qq, kk, vv, oo, ll, w.B, w.H, Sq, Sk, w.D, scale, w.causal, stream=stream, **extra)
+    # one step = the whole hot path; for fp8 the prep kernel then the attention
+    kernels = []          # (name, launch fn)
+    if fp8:
+        prep = api.fp8_prepare(q, k, v, inputs["sigma"], batch=w.B, stream=stream)
+        kernels.append(("fp8_prep_kernel", lambda: api.fa_fp8_prep(
+            q, k, v, prep["q8"], prep["k8"], prep["v8"], prep["q_scale"], prep["k_scale"], prep["v_scale"],
+            inputs["sigma"], w.B, w.H, Sq, Sk, w.D, stream=stream)))
+        kernels.append(("fa_fwd_kernel", lambda: api.fp8_attention_forward(
+            prep, causal=w.causal, scale=scale, out=o, lse=lse, stream=stream)))
+    else:
+        kernels.append(("fa_fwd_kernel", lambda: api.fa_fwd(
+            q, k, v, o, lse, w.B, w.H, Sq, Sk, w.D, scale, w.causal, stream=stream, **extra)))
+
+    def step():
+        for _, fn in kernels:
+            fn()
 
     for _ in range(args.warmup):
         step()
     api.fa_get_device_status(stream)
     ceiling = gemm_ceiling(torch, dev)
 
-    def timed(fn, steps):
+    def timed(fn, steps, per_kernel=False):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        e0, e1 = ev(), ev()
+        marks = []
         e0.record(stream)
         for _ in range(steps):
-            fn()
+            if per_kernel:
+                m = [ev() for _ in range(len(kernels) + 1)]
+                m[0].record(stream)
+                for j, (_, kf) in enumerate(kernels):
+                    kf()
+                    m[j + 1].record(stream)
+                marks.append(m)
+            else:
+                fn()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if world > 1:
@@ -307,10 +330,12 @@ def main(argv=None):
             t = torch.tensor([ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ms = float(t.item())
-        return ms
+        per = [sum(m[j].elapsed_time(m[j + 1]) for m in marks) / max(1, len(marks))
+               for j in range(len(kernels))] if per_kernel else None
+        return ms, per
 
     with ClockSampler(local) as clk:
-        total_ms = timed(step, args.steps)
+        total_ms, per_kernel = timed(step, args.steps, per_kernel=True)
     api.fa_get_device_status(stream)
     ms_per_step = total_ms / args.steps
     value = world * flops / (ms_per_step * 1e-3) / 1e12
@@ -331,38 +356,54 @@ def main(argv=None):
     for _ in range(3):
         e2e_step()
     e2e_steps = max(3, min(args.steps, 50))
-    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
+    e2e_ms = timed(e2e_step, e2e_steps)[0] / e2e_steps
     api.fa_get_device_status(stream)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"]
-    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    attn_ms = per_kernel[-1]
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    if fp8:
+        peak = peaks["bf16_tflops"] * 2.0
+        peak_note = (f"{peak_src} bf16 dense GEMM (burst) x 2, the nominal fp8/bf16 dense ratio "
+                     "(4.5 / 2.25 PFLOP/s)")
+    else:
+        peak = peaks["bf16_tflops"]
+        peak_note = f"{peak_src} bf16 dense GEMM (burst), MEASURED_PEAKS.json"
     kern = "fa_fwd_kernel"
-    traffic = committed_traffic(kern, w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": Sq, "Sk": Sk, "D": w.D,
                    "causal": w.causal, "varlen": w.varlen, "scale": scale,
                    "l2": "inputs larger than L2 (no flush between steps)",
-                   "inputs": "Q,K,V iid N(0,1) fp32 -> %s, seed %d" % (w.dtype, w.seed)},
+                   "inputs": "Q,K,V iid N(0,1) fp32 -> %s, seed %d%s" % (
+                       "bf16" if fp8 else w.dtype, w.seed,
+                       ", 0.1%% N(0,10^2) outliers in 4 columns, prep + attention per step" if fp8 else "")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 dense GEMM (burst), MEASURED_PEAKS.json",
-                     "kernel": kern},
-        "ceiling_in_run": {"bf16_gemm_tflops": ceiling, "frac": achieved / ceiling},
+                     "frac": achieved / peak, "traffic": committed_traffic(kern, w.name),
+                     "peak_source": peak_note, "kernel": kern, "kernel_ms": attn_ms},
+        "ceiling_in_run": {"bf16_gemm_tflops": ceiling,
+                           "frac": achieved / (ceiling * (2.0 if fp8 else 1.0))},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * len(kernels),
         "clocks": clk.summary(),
     }
+    if fp8:
+        pb = A.prep_bytes(w.H, w.D, w.B, w.Sq)
+        gbs = pb / (per_kernel[0] * 1e-3) / 1e9
+        line["prep_roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / peaks["hbm_gbs"], "kernel": "fp8_prep_kernel",
+                                 "kernel_ms": per_kernel[0], "bytes": pb,
+                                 "traffic": committed_traffic("fp8_prep_kernel", w.name)}
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         cb = oracle_sample(w, {"q": q.cpu(), "k": k.cpu(), "v": v.cpu(),
                                "cu_seqlens_q": inputs["cu_seqlens_q"]}, seconds=args.cpu_seconds)
         cb.pop("seconds")
+        cb.pop("rows")
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)

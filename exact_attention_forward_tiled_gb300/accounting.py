@@ -39,9 +39,10 @@ def attention_bytes(H, D, Tq, Tk, in_dtype, out_dtype="bf16", n_lse=None) -> flo
     return H * D * (Tq * eb + 2 * Tk * eb + Tq * ob) + 4.0 * n_lse
 
 
-def prep_bytes(H, D, T, in_dtype="bf16") -> float:
-    """FP8 prep: read three [T, H, D] 16-bit tensors, write three e4m3 tensors
-    and three fp32 scale arrays (one per 128-row block of each head)."""
+def prep_bytes(H, D, B, S, in_dtype="bf16") -> float:
+    """FP8 prep of Q, K, V (B sequences of S rows each): read three
+    [B*S, H, D] 16-bit tensors, write three e4m3 tensors and three fp32 scale
+    arrays (one per 128-row block of each (sequence, head))."""
     eb = ELEM_BYTES[in_dtype]
-    nblk = (T + 127) // 128
-    return 3.0 * (T * H * D * (eb + 1)) + 3.0 * 4 * H * nblk
+    nblk = B * ((S + 127) // 128)
+    return 3.0 * (B * S * H * D * (eb + 1)) + 3.0 * 4 * H * nblk

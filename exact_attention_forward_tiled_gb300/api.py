@@ -47,6 +47,10 @@ def lib():
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, i, i, i, vp]
+        L.fa_fp8_prep.restype = i
+        L.fa_fp8_prep.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        L.fa_fwd_fp8.restype = i
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_get_device_status.restype = i
         L.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i)]
         L.fa_strerror.restype = ctypes.c_char_p
@@ -87,6 +91,65 @@ def fa_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q=None, c
     if check and st != FA_OK:
         raise FAError(st, "fa_fwd")
     return st
+
+
+def fa_fp8_prep(q, k, v, q8, k8, v8, q_scale, k_scale, v_scale, sigma, B, H, Sq, Sk, D, in_dtype=None,
+                stream=None, check=True) -> int:
+    """Raw entry point: Hadamard rotation (``sigma`` int8 +-1, or None for
+    none) and per-128-row-block e4m3 quantisation of Q, K (rotated) and V."""
+    if in_dtype is None:
+        in_dtype = _DTYPE[q.dtype]
+    st = lib().fa_fp8_prep(_ptr(q), _ptr(k), _ptr(v), int(in_dtype), _ptr(q8), _ptr(k8), _ptr(v8),
+                           _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(sigma), int(B), int(H), int(Sq),
+                           int(Sk), int(D), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fp8_prep")
+    return st
+
+
+def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, Sq, Sk, D, scale, causal, stream=None,
+               check=True) -> int:
+    """Raw entry point: attention on e4m3 codes with block scales; bf16 O."""
+    st = lib().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(o),
+                          _ptr(lse), int(B), int(H), int(Sq), int(Sk), int(D), float(scale), int(bool(causal)),
+                          _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
+    return st
+
+
+def fp8_prepare(q, k, v, sigma, *, batch, stream=None):
+    """Allocate the e4m3 tensors and block scales and call ``fa_fp8_prep``.
+    q ``[B*Sq, H, D]``, k/v ``[B*Sk, H, D]`` 16-bit. Returns a dict."""
+    B = batch
+    H, D = q.shape[1], q.shape[2]
+    Sq, Sk = q.shape[0] // B, k.shape[0] // B
+    dev = q.device
+    out = {"q8": torch.empty(q.shape, dtype=torch.uint8, device=dev),
+           "k8": torch.empty(k.shape, dtype=torch.uint8, device=dev),
+           "v8": torch.empty(v.shape, dtype=torch.uint8, device=dev),
+           "q_scale": torch.empty((B, H, (Sq + 127) // 128), dtype=torch.float32, device=dev),
+           "k_scale": torch.empty((B, H, (Sk + 127) // 128), dtype=torch.float32, device=dev),
+           "v_scale": torch.empty((B, H, (Sk + 127) // 128), dtype=torch.float32, device=dev),
+           "B": B, "H": H, "Sq": Sq, "Sk": Sk, "D": D}
+    fa_fp8_prep(q, k, v, out["q8"], out["k8"], out["v8"], out["q_scale"], out["k_scale"], out["v_scale"],
+                sigma, B, H, Sq, Sk, D, stream=stream)
+    return out
+
+
+def fp8_attention_forward(prep, *, causal=False, scale=None, out=None, lse=None, stream=None):
+    """Attention on the output of ``fp8_prepare``; returns (O bf16, LSE fp32)."""
+    B, H, Sq, Sk, D = prep["B"], prep["H"], prep["Sq"], prep["Sk"], prep["D"]
+    if scale is None:
+        scale = D ** -0.5
+    dev = prep["q8"].device
+    if out is None:
+        out = torch.empty((B * Sq, H, D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    fa_fwd_fp8(prep["q8"], prep["k8"], prep["v8"], prep["q_scale"], prep["k_scale"], prep["v_scale"], out, lse,
+               B, H, Sq, Sk, D, scale, causal, stream=stream)
+    return out, lse
 
 
 def fa_get_device_status(stream=None, check=True):

@@ -167,9 +167,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   L.p.ntiles = (int)ntiles;
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
-  L.p.tile_counter = nullptr;
   L.D = D;
-  L.fp16 = dtype == FA_FP16;
+  L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
   L.causal = causal != 0;
   L.num_sms = dev->sms;
   L.stream = static_cast<cudaStream_t>(stream);
@@ -180,6 +179,117 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     case 128: e = fa::launch_fwd_d128(L); break;
     default: e = fa::launch_fwd_d256(L); break;
   }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype, void* q8, void* k8, void* v8,
+                float* q_scale, float* k_scale, float* v_scale, const signed char* sigma, int B, int H,
+                int Sq, int Sk, int D, void* stream) {
+  if (in_dtype != FA_FP16 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if ((int64_t)B * Sq > INT32_MAX || (int64_t)B * Sk > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (B == 0 || (Sq == 0 && Sk == 0)) return FA_OK;
+  const bool has_q = Sq > 0, has_kv = Sk > 0;
+  if ((has_q && (!q || !q8 || !q_scale)) || (has_kv && (!k || !v || !k8 || !v8 || !k_scale || !v_scale)))
+    return FA_ERR_INVALID_ARG;
+  const void* ptrs16[3] = {q, k, v};
+  for (const void* p : ptrs16)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return FA_ERR_ALIGNMENT;
+  const void* ptrs8[3] = {q8, k8, v8};
+  for (const void* p : ptrs8)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return FA_ERR_ALIGNMENT;
+  const void* ptrs32[3] = {q_scale, k_scale, v_scale};
+  for (const void* p : ptrs32)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return FA_ERR_ALIGNMENT;
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+  fa::PrepParams t[3];
+  int n = 0;
+  auto add = [&](const void* x, void* x8, float* sc, const signed char* sg, int S) {
+    fa::PrepParams& P = t[n++];
+    P.x = x;
+    P.x8 = static_cast<uint8_t*>(x8);
+    P.scale = sc;
+    P.sigma = reinterpret_cast<const int8_t*>(sg);
+    P.B = B;
+    P.H = H;
+    P.S = S;
+    P.nblk = (S + 127) / 128;
+    P.bf16 = in_dtype == FA_BF16;
+  };
+  if (has_q) add(q, q8, q_scale, sigma, Sq);
+  if (has_kv) {
+    add(k, k8, k_scale, sigma, Sk);
+    add(v, v8, v_scale, nullptr, Sk);
+  }
+  cudaError_t e = fa::launch_fp8_prep(t, n, D, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
+               int causal, void* stream) {
+  if (D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const int64_t Tq = (int64_t)B * Sq, Tk = (int64_t)B * Sk;
+  if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return FA_OK;
+  if (!q8 || !k8 || !v8 || !o || !lse || !q_scale || (Sk > 0 && (!k_scale || !v_scale)))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return FA_ERR_ALIGNMENT;
+  const int rows = fa::cta_rows(D);
+  const int64_t n_qblk = ((int64_t)Sq + rows - 1) / rows;
+  const int64_t ntiles = (int64_t)B * H * n_qblk;
+  if (ntiles > INT32_MAX || (int64_t)B * H * Sq > ((int64_t)1 << 40)) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  const uint64_t cols = (uint64_t)H * D;
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if ((st = make_map(&L.tq, q8, dt, 1, cols, (uint64_t)Tq, 128, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tk, k8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tv, v8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
+  L.p.o = o;
+  L.p.lse = lse;
+  L.p.B = B;
+  L.p.H = H;
+  L.p.Sq = Sq;
+  L.p.Sk = Sk;
+  L.p.total_q = (int)Tq;
+  L.p.total_k = (int)Tk;
+  L.p.n_qblk = (int)n_qblk;
+  L.p.ntiles = (int)ntiles;
+  L.p.c = (float)((double)scale * 1.4426950408889634);
+  L.p.status = dev->status;
+  L.p.q_scale = q_scale;
+  L.p.k_scale = k_scale;
+  L.p.v_scale = v_scale;
+  L.p.nblk_q = (Sq + 127) / 128;
+  L.p.nblk_k = (Sk + 127) / 128;
+  L.D = D;
+  L.kind = fa::kE4M3;
+  L.causal = causal != 0;
+  L.num_sms = dev->sms;
+  L.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 128 ? fa::launch_fwd_fp8_d128(L) : fa::launch_fwd_fp8_d256(L);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;

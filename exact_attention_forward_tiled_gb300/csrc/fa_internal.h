@@ -27,15 +27,23 @@ struct FwdParams {
   int ntiles;              // B * H * n_qblk
   float c;                 // softmax scale * log2(e)
   int* status;             // device status word
-  uint32_t* tile_counter;  // unused by the static scheduler (reserved)
+  // e4m3 inputs only: fp32 block scales [B, H, nblk] of Q', K', V (one per
+  // 128-row block of a head); real value = code value * scale
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int nblk_q, nblk_k;
 };
+
+// Element kinds of the attention inputs.
+enum Kind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 // Per-launch description filled by the front end.
 struct FwdLaunch {
   CUtensorMap tq, tk, tv;
   FwdParams p;
   int D;
-  bool fp16;
+  int kind;  // Kind
   bool causal;
   int num_sms;
   cudaStream_t stream;
@@ -47,5 +55,18 @@ constexpr int cta_rows(int D) { return D <= 128 ? 256 : 128; }
 cudaError_t launch_fwd_d64(const FwdLaunch& L);
 cudaError_t launch_fwd_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_d256(const FwdLaunch& L);
+cudaError_t launch_fwd_fp8_d128(const FwdLaunch& L);
+cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
+
+// FP8 preparation: rotation (optional) + block quantisation of one tensor.
+struct PrepParams {
+  const void* x;        // [B*S, H, D] 16-bit input
+  uint8_t* x8;          // [B*S, H, D] e4m3 output
+  float* scale;         // [B, H, nblk] fp32 output
+  const int8_t* sigma;  // [D] +-1, or nullptr: no rotation
+  int B, H, S, nblk;
+  int bf16;             // 1: bf16 input, 0: fp16
+};
+cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cudaStream_t stream);
 
 }  // namespace fa

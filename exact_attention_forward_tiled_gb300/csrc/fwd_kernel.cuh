@@ -12,25 +12,30 @@
 //
 //   softmax warpgroups (4 warps per query tile, thread r owns row r)
 //       tcgen05.ld the fp32 score row from tensor memory, mask, row max,
-//       lazy rescale of O (only when the row max grows by more than TAU in
-//       log2 units), P = exp2(S * scale * log2 e - m), row sum, P -> 16-bit,
-//       tcgen05.st P back into tensor memory over its scores; at the end of
-//       the work tile O / l and LSE are written to global memory.
+//       lazy rescale of O (only when the row max grows by more than kTau in
+//       log2 units), P = exp2(S * scale * log2 e - m), row sum, P -> 16-bit
+//       (or e4m3), tcgen05.st P back into tensor memory over its scores; at
+//       the end of the work tile O / l and LSE are written to global memory.
 //   MMA warp (one thread)
-//       tcgen05.mma kind::f16: S_t = Q_t K_j^T (both operands in shared
-//       memory) and O_t += P_t V_j (P from tensor memory, V from shared
-//       memory), accumulators in tensor memory; tcgen05.commit signals
-//       mbarriers. For QT = 2 the issue order QK0_j, PV1_{j-1}, QK1_j, PV0_j
-//       keeps the tensor core busy while the two softmax warpgroups take
-//       turns (the ping-pong idea of the FlashAttention-3 wiki, technique 1,
-//       done with two tensor-memory score buffers instead of two register
-//       files).
+//       tcgen05.mma: S_t = Q_t K_j^T (both operands in shared memory) and
+//       O_t += P_t V_j (P from tensor memory, V from shared memory),
+//       accumulators in tensor memory; tcgen05.commit signals mbarriers. For
+//       QT = 2 the issue order QK0_j, PV1_{j-1}, QK1_j, PV0_j keeps the tensor
+//       core busy while the two softmax warpgroups take turns (the ping-pong
+//       of the FlashAttention-3 wiki, technique 1, done with two tensor-memory
+//       score buffers instead of two register files).
 //   load warp (one thread)
 //       TMA loads of the Q tiles and of K_j, V_j into a ring of shared-memory
 //       slots guarded by full / empty mbarriers (producer / consumer of the
 //       wiki's technique 1; multi-stage K/V pipeline of technique 2).
 //
-// Every wait on an mbarrier is bounded: after WAIT_LIMIT_NS the waiting role
+// Input kinds: fp16 or bf16 (tcgen05 kind::f16, 16 keys per MMA step), or
+// e4m3 with per-128-row-block scales (kind::f8f6f4, 32 keys per step; the
+// FlashAttention-3 wiki, technique 3). For e4m3 the block scales are folded
+// into the per-tile softmax constant (q_s * k_s) and into P (v_s relative to
+// the head's largest V scale) so the MMAs run on raw codes.
+//
+// Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting role
 // records a timeout in the device status word, raises an abort flag that the
 // other roles see, and all roles leave; tensor memory is freed on the way out.
 #pragma once
@@ -43,23 +48,40 @@
 
 namespace fa {
 
-constexpr float kTau = 8.0f;                      // lazy-rescale threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D_, int QT_, int STAGES_>
+template <int D_, int QT_, int STAGES_, int KIND_>
 struct FwdCfg {
   static constexpr int D = D_;
   static constexpr int QT = QT_;
   static constexpr int STAGES = STAGES_;
-  static constexpr int kRows = 128 * QT;          // query rows per work tile
-  static constexpr int kBoxes = D / 64;           // 64-element (128-byte) column boxes
-  static constexpr int kBoxBytes = 128 * 128;     // one box: 128 rows x 128 bytes
+  static constexpr int KIND = KIND_;
+  static constexpr bool kFp8 = KIND == kE4M3;
+  static constexpr int EB = kFp8 ? 1 : 2;          // bytes per input element
+  static constexpr int kRows = 128 * QT;            // query rows per work tile
+  static constexpr int kBoxCols = 128 / EB;         // elements per 128-byte box row
+  static constexpr int kBoxes = D / kBoxCols;       // boxes per 128-row tile
+  static constexpr int kBoxBytes = 128 * 128;       // one box: 128 rows x 128 bytes
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kQkSteps = D * EB / 32;      // MMA K steps (32 bytes each) over D
+  static constexpr int kKeysPerStep = 32 / EB;      // keys per PV MMA step
+  static constexpr int kPvSteps = 128 / kKeysPerStep;
+  // lazy-rescale threshold (log2 units) and, for e4m3, the power of two P is
+  // scaled by before it is rounded (P * 2^kappa <= 2^(tau + kappa) = 256 < 448)
+  static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
+  static constexpr float kKappaScale = kFp8 ? 16.0f : 1.0f;
+  static constexpr float kLog2Kappa = kFp8 ? 4.0f : 0.0f;
   static constexpr int kSoftmaxWarps = 4 * QT;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kLoadWarp = kSoftmaxWarps + 1;
-  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+  // QT = 2: a third warpgroup (MMA warp, load warp, two idle warps) gives its
+  // registers to the two softmax warpgroups: 384 threads launch at 168
+  // registers each (64512); 128 x 64 + 256 x 216 = 63488 <= 64512.
+  static constexpr bool kRebalance = QT == 2;
+  static constexpr int kRegsLow = 64, kRegsHigh = 216;
+  static constexpr int kThreads = kRebalance ? 384 : 32 * (kSoftmaxWarps + 2);
+  static_assert(!kRebalance || kThreads * 168 >= 128 * kRegsLow + 256 * kRegsHigh, "register split");
   static constexpr int kTmemCols = 512;
   // tensor-memory columns: score buffers S0, S1; accumulators O0 (, O1)
   __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return b ? 128u : 0u; }
@@ -78,6 +100,7 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 
   static_assert(D == 64 || D == 128 || D == 256, "head dimension");
+  static_assert(D % kBoxCols == 0, "a 128-row tile must be whole 128-byte boxes");
   static_assert(QT == 1 || 2 * 128 + QT * D <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -85,11 +108,12 @@ struct FwdCfg {
 // Work tile: CTA query block of one (sequence, head).
 struct TileInfo {
   int b, h;
-  int q0;        // first query row of the block within its sequence
-  int Lq, Lk;    // sequence lengths
+  int qblk;        // CTA query block index within the sequence
+  int q0;          // first query row of the block within its sequence
+  int Lq, Lk;      // sequence lengths
   int qtok, ktok;  // token index of row 0 of the sequence in Q/O and in K/V
-  int n_kv;      // key blocks of 128 to visit
-  bool live;     // false: the block starts beyond the sequence
+  int n_kv;        // key blocks of 128 to visit
+  bool live;       // false: the block starts beyond the sequence
 };
 
 // Heads are the outer loop so that the CTAs running at the same time share
@@ -101,6 +125,7 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   const int bh = w / p.n_qblk;
   const int j = w - bh * p.n_qblk;
   const int qblk = CAUSAL ? (p.n_qblk - 1 - j) : j;
+  t.qblk = qblk;
   t.b = bh / p.H;
   t.h = bh - t.b * p.H;
   if (p.cu_q != nullptr) {
@@ -182,7 +207,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   auto load_tile = [&](const CUtensorMap* m, int h, int row, uint32_t dst, uint32_t b) {
 #pragma unroll
     for (int bx = 0; bx < C::kBoxes; ++bx)
-      ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * 64, row, b);
+      ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
   };
   auto load_kv = [&](const CUtensorMap* m, int h, int row) -> bool {
     const int s = kvc % C::STAGES;
@@ -229,33 +254,42 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
 }
 
 // ------------------------------------------------------------------ MMA warp
-template <class C, bool FP16, bool CAUSAL>
+template <class C, bool CAUSAL>
 __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
-  constexpr uint32_t fmt = FP16 ? 0u : 1u;
+  // operand format field: kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = e4m3
+  constexpr uint32_t fmt = C::KIND == kBF16 ? 1u : 0u;
   constexpr uint32_t idesc_qk = ptx::make_idesc(fmt, false, 128, 128);
   constexpr uint32_t idesc_pv = ptx::make_idesc(fmt, true, 128, C::D);
   const uint32_t sq = sbase + C::kOffQ;
   auto slot_addr = [&](uint32_t c) { return sbase + C::kOffKV + (c % C::STAGES) * C::kTileBytes; };
   auto slot = [&](uint32_t c) { return (int)(c % C::STAGES); };
 
-  // S[s_col] = Q_t K^T : D/16 steps of K = 16 along the head dimension
+  // S[s_col] = Q_t K^T : steps of 32 bytes of the head dimension (16 f16 or 32 e4m3)
   auto qk = [&](uint32_t s_col, uint32_t q_addr, uint32_t k_addr) {
 #pragma unroll
-    for (int kk = 0; kk < C::D / 16; ++kk) {
+    for (int kk = 0; kk < C::kQkSteps; ++kk) {
       const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-      ptx::mma_f16_ss(tmem + s_col, ptx::smem_desc_sw128(q_addr + off, 16, 1024),
-                      ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
+      const uint64_t a = ptx::smem_desc_sw128(q_addr + off, 16, 1024);
+      const uint64_t b = ptx::smem_desc_sw128(k_addr + off, 16, 1024);
+      if (C::kFp8)
+        ptx::mma_f8_ss(tmem + s_col, a, b, idesc_qk, kk > 0);
+      else
+        ptx::mma_f16_ss(tmem + s_col, a, b, idesc_qk, kk > 0);
     }
   };
-  // O[o_col] (+)= P[p_col] V : 8 steps of K = 16 keys; P packs 2 keys per column
+  // O[o_col] (+)= P[p_col] V : steps of kKeysPerStep keys; 8 P columns per step
   auto pv = [&](uint32_t o_col, uint32_t p_col, uint32_t v_addr, bool acc) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      ptx::mma_f16_ts(tmem + o_col, tmem + p_col + kk * 8,
-                      ptx::smem_desc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
-                      (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < C::kPvSteps; ++kk) {
+      const uint64_t b =
+          ptx::smem_desc_sw128(v_addr + kk * C::kKeysPerStep * 128, C::kBoxBytes, 1024);
+      const uint32_t en = (acc || kk > 0) ? 1u : 0u;
+      if (C::kFp8)
+        ptx::mma_f8_ts(tmem + o_col, tmem + p_col + kk * 8, b, idesc_pv, en);
+      else
+        ptx::mma_f16_ts(tmem + o_col, tmem + p_col + kk * 8, b, idesc_pv, en);
     }
   };
   auto kv_ready = [&](uint32_t c) {
@@ -344,20 +378,25 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
 }
 
 // ------------------------------------------------------------------ softmax warpgroups
-template <bool FP16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  return FP16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
+template <int KIND>
+__device__ __forceinline__ uint32_t pack_out(float lo, float hi) {
+  // output element pair: fp16 for fp16 inputs, bf16 otherwise (e4m3 -> bf16 O)
+  return KIND == kF16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
 }
 
-template <class C, bool FP16, bool CAUSAL>
+template <int KIND>
+__device__ __forceinline__ uint32_t pack_p16(float lo, float hi) {
+  return KIND == kF16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
+}
+
+template <class C, bool CAUSAL>
 __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
                              int t, int quarter) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   const int lane = threadIdx.x & 31;
-  const int r = quarter * 32 + lane;                         // row within the 128-row tile
+  const int r = quarter * 32 + lane;                            // row within the 128-row tile
   const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
-  const float c = p.c;
   const float NEG_INF = -CUDART_INF_F;
 
   uint32_t it = 0, tcount = 0;
@@ -379,46 +418,61 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
       }
       continue;
     }
+    // e4m3: per-tile score constant c * q_s * k_s(j); P weight v_s(j) / v_ref
+    float c_q = p.c, v_ref = 1.f;
+    const float* ks_row = nullptr;
+    const float* vs_row = nullptr;
+    if (C::kFp8) {
+      const int64_t hb = (int64_t)ti.b * p.H + ti.h;
+      c_q = p.c * __ldg(p.q_scale + hb * p.nblk_q + min(ti.qblk * C::QT + t, p.nblk_q - 1));
+      ks_row = p.k_scale + hb * p.nblk_k;
+      vs_row = p.v_scale + hb * p.nblk_k;
+      float vmax = 0.f;
+      for (int j = 0; j < p.nblk_k; ++j) vmax = fmaxf(vmax, __ldg(vs_row + j));
+      v_ref = vmax > 0.f ? vmax : 1.f;
+    }
+    const float inv_vref = 1.f / v_ref;
     const int key_lim = CAUSAL ? min(ti.Lk, row + ti.Lk - ti.Lq + 1) : ti.Lk;
     float m_ref = NEG_INF, l = 0.f;
     bool ok = true;
     for (int i = 0; i < ti.n_kv; ++i, ++it) {
+      const float c = C::kFp8 ? c_q * __ldg(ks_row + i) : c_q;
+      // log2 of the factor the stored P carries: 2^kappa * v_s(j) / v_ref (e4m3 only)
+      const float lg_pw = C::kFp8 ? ptx::lg2(__ldg(vs_row + i) * inv_vref) + C::kLog2Kappa : 0.f;
       const int buf = C::QT == 2 ? t : (int)(it & 1u);
       const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
       if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;
       ptx::tc_fence_after();
       const uint32_t s_addr = tl + C::col_s(buf);
+      uint32_t sv[128];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * ch));
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) ptx::reg_fence(*reinterpret_cast<uint32_t(*)[32]>(sv + 32 * ch));
       float s[128];
-      {
-        uint32_t v[32];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          ptx::tmem_ld32(s_addr + 32 * ch, v);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[32 * ch + j] = __uint_as_float(v[j]);
-        }
-      }
+      for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sv[j]);
       const int lim_local = key_lim - 128 * i;
-      const bool masked = lim_local < 128;   // keys j >= lim_local are not visible
+      const bool masked = lim_local < 128;  // keys j >= lim_local are not visible
       if (masked) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = j < lim_local ? s[j] : NEG_INF;
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = s[a];
+      for (int a = 0; a < 4; ++a) mx[a] = fmaxf(s[a], s[a + 4]);
 #pragma unroll
       for (int j = 8; j < 128; j += 8)
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(mx[a], s[j + a]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int a = 0; a < 4; ++a) mx[a] = ptx::max3(mx[a], s[j + a], s[j + 4 + a]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_tile = mt == NEG_INF ? NEG_INF : mt * c;  // scaled log2 units (c >= 0)
       if (i == 0) {
         m_ref = m_tile;
       } else {
-        const bool need = m_tile > m_ref + kTau;
+        const bool need = m_tile > m_ref + C::kTau;
         if (__any_sync(0xffffffffu, need)) {
           if (C::QT == 1) {
             // the previous PV must have landed in O before it is rescaled
@@ -430,40 +484,73 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
             m_ref = m_tile;
             l *= alpha;
           }
+          const uint64_t a2 = ptx::f2pack(alpha, alpha);
           const uint32_t o_addr = tl + C::col_o(t);
 #pragma unroll 1
           for (int ch = 0; ch < C::D / 32; ++ch) {
             uint32_t v[32];
             ptx::tmem_ld32(o_addr + 32 * ch, v);
             ptx::tmem_wait_ld();
+            ptx::reg_fence(v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            for (int j = 0; j < 32; j += 2) {
+              float lo, hi;
+              ptx::f2unpack(ptx::mul2(ptx::f2pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), a2),
+                            lo, hi);
+              v[j] = __float_as_uint(lo);
+              v[j + 1] = __float_as_uint(hi);
+            }
             ptx::tmem_st32(o_addr + 32 * ch, v);
           }
           ptx::tmem_wait_st();
         }
       }
-      const float mu = m_ref == NEG_INF ? 0.f : m_ref;
+      // exponent argument s * c - m (+ log2 of the e4m3 P weight), two lanes at a time
+      const float mu = (m_ref == NEG_INF ? 0.f : m_ref) - lg_pw;
+      const uint64_t c2 = ptx::f2pack(c, c), nm2 = ptx::f2pack(-mu, -mu);
 #pragma unroll
-      for (int j = 0; j < 128; ++j) s[j] = ptx::ex2(fmaf(s[j], c, -mu));
+      for (int j = 0; j < 128; j += 2) {
+        float lo, hi;
+        ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
+        s[j] = ptx::ex2(lo);
+        s[j + 1] = ptx::ex2(hi);
+      }
       if (masked) {
         // zero the invisible keys after the exponent: with c = 0 their
         // -inf * c would be NaN
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = j < lim_local ? s[j] : 0.f;
       }
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int j = 0; j < 128; ++j) ls[j & 3] += s[j];
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      for (int j = 0; j < 128; j += 2)
+        acc[(j >> 1) & 3] = ptx::add2(acc[(j >> 1) & 3], ptx::f2pack(s[j], s[j + 1]));
+      {
+        float a0, a1, b0, b1, c0, c1, d0, d1;
+        ptx::f2unpack(acc[0], a0, a1);
+        ptx::f2unpack(acc[1], b0, b1);
+        ptx::f2unpack(acc[2], c0, c1);
+        ptx::f2unpack(acc[3], d0, d1);
+        const float tile_sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        // e4m3: the stored P carries the weight 2^lg_pw; l sums unweighted P
+        l += C::kFp8 ? tile_sum * ptx::ex2(-lg_pw) : tile_sum;
+      }
       {
         uint32_t pk[32];
+        if (C::kFp8) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack2<FP16>(s[2 * j], s[2 * j + 1]);
-        ptx::tmem_st32(s_addr, pk);
+          for (int j = 0; j < 32; ++j)
+            pk[j] = ptx::pack_e4m3x2(s[4 * j], s[4 * j + 1]) |
+                    (ptx::pack_e4m3x2(s[4 * j + 2], s[4 * j + 3]) << 16);
+          ptx::tmem_st32(s_addr, pk);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack2<FP16>(s[64 + 2 * j], s[64 + 2 * j + 1]);
-        ptx::tmem_st32(s_addr + 32, pk);
+          for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[2 * j], s[2 * j + 1]);
+          ptx::tmem_st32(s_addr, pk);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[64 + 2 * j], s[64 + 2 * j + 1]);
+          ptx::tmem_st32(s_addr + 32, pk);
+        }
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -471,21 +558,22 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + buf));
     }
     if (!ok) return;
-    // epilogue: O / l, LSE
+    // epilogue: O / l (e4m3: O * v_ref * 2^-kappa / l), LSE
     if (!wt.wait_warp(bar(C::kBarOFull + (C::QT == 2 ? t : 0)), tcount & 1u, 7)) return;
     ++tcount;
     ptx::tc_fence_after();
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const float inv_l = l > 0.f ? (C::kFp8 ? v_ref / (C::kKappaScale * l) : 1.f / l) : 0.f;
     const uint32_t o_addr = tl + C::col_o(C::QT == 2 ? t : 0);
 #pragma unroll 1
     for (int ch = 0; ch < C::D / 32; ++ch) {
       uint32_t v[32];
       ptx::tmem_ld32(o_addr + 32 * ch, v);
       ptx::tmem_wait_ld();
+      ptx::reg_fence(v);
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        pk[j] = pack2<FP16>(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
+        pk[j] = pack_out<C::KIND>(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
       if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
 #pragma unroll
@@ -499,11 +587,11 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int QT, int STAGES, bool FP16, bool CAUSAL>
-__global__ void __launch_bounds__(FwdCfg<D, QT, STAGES>::kThreads, 1)
+template <int D, int QT, int STAGES, int KIND, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using C = FwdCfg<D, QT, STAGES>;
+  using C = FwdCfg<D, QT, STAGES, KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -535,13 +623,18 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const Waiter wt{abort_flag, p.status};
-
-  if (warp == C::kLoadWarp) {
-    if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt);
-  } else if (warp == C::kMmaWarp) {
-    if (lane == 0) mma_role<C, FP16, CAUSAL>(p, sbase, tmem, wt);
+  // each role runs inside the branch that set its register budget, so the
+  // register allocator sees one budget per role
+  if (warp >= C::kSoftmaxWarps) {
+    if constexpr (C::kRebalance) ptx::setmaxnreg_dec<C::kRegsLow>();
+    if (warp == C::kLoadWarp) {
+      if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt);
+    } else if (warp == C::kMmaWarp) {
+      if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt);
+    }
   } else {
-    softmax_role<C, FP16, CAUSAL>(p, sbase, tmem, wt, warp >> 2, warp & 3);
+    if constexpr (C::kRebalance) ptx::setmaxnreg_inc<C::kRegsHigh>();
+    softmax_role<C, CAUSAL>(p, sbase, tmem, wt, warp >> 2, warp & 3);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -552,20 +645,22 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES>::kThreads, 1)
   }
 }
 
-template <int D, int QT, int STAGES>
-cudaError_t launch_fwd_impl(const FwdLaunch& L) {
-  using C = FwdCfg<D, QT, STAGES>;
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams);
-  if (L.fp16)
-    kern = L.causal ? fa_fwd_kernel<D, QT, STAGES, true, true> : fa_fwd_kernel<D, QT, STAGES, true, false>;
-  else
-    kern = L.causal ? fa_fwd_kernel<D, QT, STAGES, false, true> : fa_fwd_kernel<D, QT, STAGES, false, false>;
+template <int D, int QT, int STAGES, int KIND>
+cudaError_t launch_fwd_kind(const FwdLaunch& L) {
+  using C = FwdCfg<D, QT, STAGES, KIND>;
+  auto kern = L.causal ? fa_fwd_kernel<D, QT, STAGES, KIND, true> : fa_fwd_kernel<D, QT, STAGES, KIND, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   int grid = L.p.ntiles < L.num_sms ? L.p.ntiles : L.num_sms;
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tq, L.tk, L.tv, L.p);
   return cudaGetLastError();
+}
+
+// 16-bit inputs: fp16 or bf16
+template <int D, int QT, int STAGES>
+cudaError_t launch_fwd_impl(const FwdLaunch& L) {
+  return L.kind == kF16 ? launch_fwd_kind<D, QT, STAGES, kF16>(L) : launch_fwd_kind<D, QT, STAGES, kBF16>(L);
 }
 
 }  // namespace fa

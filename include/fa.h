@@ -67,7 +67,7 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
  *                varlen only: rows of q/o and of k/v (cu_seqlens[B] may not
  *                exceed them); ignored for fixed length
  *   dtype        FA_FP16 or FA_BF16 (FA_FP8_E4M3 -> FA_ERR_UNSUPPORTED; the
- *                8-bit path has its own entry points)
+ *                8-bit path is fa_fp8_prep + fa_fwd_fp8 below)
  *
  * A varlen sequence whose lengths break the bounds is skipped on the device
  * and reported as FA_ERR_DEVICE_SEQLENS by fa_get_device_status().
@@ -76,6 +76,46 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Sq, int Sk, int D, float scale, int causal,
            const int* cu_seqlens_q, const int* cu_seqlens_k, int total_q, int total_k,
            int dtype, void* stream);
+
+/*
+ * fa_fp8_prep -- FP8 preparation of the inputs ("FlashAttention-3 (lukebest
+ * wiki)", technique 3: block quantisation and incoherent processing).
+ *
+ *   q, k, v      16-bit inputs, [B*Sq, H, D] and [B*Sk, H, D] (in_dtype
+ *                FA_FP16 or FA_BF16), fixed length
+ *   q8, k8, v8   e4m3 outputs, same shapes, one byte per element (written)
+ *   q_scale      fp32 [B, H, ceil(Sq/128)] (written); k_scale, v_scale
+ *                fp32 [B, H, ceil(Sk/128)] (written)
+ *   sigma        device int8 [D] of +-1, or NULL for no rotation
+ *   D            64, 128 or 256
+ *
+ * Q' = Q M and K' = K M with M = diag(sigma) H_D / sqrt(D) (H_D the
+ * Sylvester Hadamard matrix in natural order; M is orthogonal so
+ * Q'K'^T = QK^T); V is not rotated. For every 128-row block of every
+ * (sequence, head) of Q', K' and V: scale = amax / 448 (1.0 for an all-zero
+ * block) and code = e4m3(x / scale), round to nearest even, saturating at
+ * +-448 (the "fn" encoding, no infinities). Sq = 0 or Sk = 0 skips those
+ * tensors (their pointers may then be NULL).
+ */
+int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype,
+                void* q8, void* k8, void* v8, float* q_scale, float* k_scale, float* v_scale,
+                const signed char* sigma, int B, int H, int Sq, int Sk, int D, void* stream);
+
+/*
+ * fa_fwd_fp8 -- attention forward on the output of fa_fp8_prep: the same
+ * operation as fa_fwd on the dequantised values (code * block scale), with
+ * the block scales folded into the softmax constant and into P, and P
+ * rounded to e4m3 before it multiplies V.
+ *
+ *   q8, k8, v8 and the three scale arrays as written by fa_fp8_prep
+ *   o            bf16 [B*Sq, H, D] (written); lse fp32 [B, H, Sq] (written)
+ *   D            128 or 256 (64 -> FA_ERR_UNSUPPORTED)
+ *   scale, causal as for fa_fwd. Fixed length only.
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
+               const float* q_scale, const float* k_scale, const float* v_scale,
+               void* o, float* lse, int B, int H, int Sq, int Sk, int D,
+               float scale, int causal, void* stream);
 
 /*
  * fa_get_device_status -- synchronise `stream`, then read and clear the
