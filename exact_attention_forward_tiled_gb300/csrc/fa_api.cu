@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -15,6 +16,13 @@
 // fa::kDev* codes; fa_get_device_status() reads and clears it.
 __device__ int g_fa_status;
 
+// Tile-scheduler counters {next tile, CTAs done}, one pair per launch slot.
+// A launch takes the next slot in turn; its last CTA puts the pair back to
+// zero, so a slot is ready again once its launch has finished. Up to
+// kSchedSlots launches may be in flight on one device at the same time.
+constexpr int kSchedSlots = 64;
+__device__ unsigned int g_fa_sched[kSchedSlots][2];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -23,6 +31,10 @@ struct DevInfo {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;
+  unsigned int* sched = nullptr;
+  std::atomic<unsigned int> next_slot{0};
+
+  unsigned int* take_slot() { return sched + 2 * (next_slot.fetch_add(1) % kSchedSlots); }
 };
 
 std::mutex g_mu;
@@ -51,6 +63,11 @@ int current_device(DevInfo** out) {
       return FA_ERR_CUDA;
     }
     d.status = static_cast<int*>(sym);
+    if (cudaGetSymbolAddress(&sym, g_fa_sched) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    d.sched = static_cast<unsigned int*>(sym);
     d.sms = sms;
     d.ready = true;
   }
@@ -167,6 +184,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   L.p.ntiles = (int)ntiles;
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
+  L.p.sched = dev->take_slot();
   L.D = D;
   L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
   L.causal = causal != 0;
@@ -279,6 +297,7 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_sc
   L.p.ntiles = (int)ntiles;
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
+  L.p.sched = dev->take_slot();
   L.p.q_scale = q_scale;
   L.p.k_scale = k_scale;
   L.p.v_scale = v_scale;

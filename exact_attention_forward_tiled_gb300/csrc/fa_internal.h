@@ -27,6 +27,9 @@ struct FwdParams {
   int ntiles;              // B * H * n_qblk
   float c;                 // softmax scale * log2(e)
   int* status;             // device status word
+  // dynamic tile scheduler: {next tile, CTAs done}; zero at launch, and the
+  // last CTA to finish puts both back to zero
+  unsigned int* sched;
   // e4m3 inputs only: fp32 block scales [B, H, nblk] of Q', K', V (one per
   // 128-row block of a head); real value = code value * scale
   const float* q_scale;

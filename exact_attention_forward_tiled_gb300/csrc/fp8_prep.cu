@@ -5,13 +5,11 @@
 // 128-row block of each (sequence, head): scale = amax / 448 (1 for an
 // all-zero block), code = e4m3(x / scale), round to nearest even, saturating.
 //
-// One CTA owns one 128 x D block of one tensor. Warp w holds rows
-// [w * RPW, (w + 1) * RPW) of the block; lane l holds the D/32 consecutive
-// elements d = l * VPL ... of each row, so a row is one coalesced 2*D-byte
-// load and one D-byte store. The Walsh-Hadamard transform runs in registers:
-// butterflies over the bits of d inside a lane, then across lanes with
-// shuffles. The block amax is reduced in shared memory before any code is
-// written, so each element is read from HBM once.
+// One CTA owns one 128 x D block of one tensor and keeps it in registers:
+// the Walsh-Hadamard transform runs there (butterflies over the bits of d
+// inside a lane, then across lanes with shuffles), the block amax is reduced
+// through shared memory, and only then are the codes written, so every
+// element is read from HBM once and written once.
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -26,39 +24,31 @@ struct PrepBatch {
   int n;
 };
 
-template <int D>
-__device__ __forceinline__ void load_row(const PrepParams& P, int64_t off, float (&x)[D / 32]) {
-  constexpr int VPL = D / 32;
-  const uint16_t* src = reinterpret_cast<const uint16_t*>(P.x) + off;
-  uint16_t h[VPL];
-  if constexpr (VPL == 2) {
-    const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(src));
-    h[0] = u & 0xffffu;
-    h[1] = u >> 16;
-  } else if constexpr (VPL == 4) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-    h[0] = u.x & 0xffffu; h[1] = u.x >> 16; h[2] = u.y & 0xffffu; h[3] = u.y >> 16;
-  } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// Eight consecutive 16-bit elements (16 bytes) -> fp32.
+__device__ __forceinline__ void load8(const PrepParams& P, int64_t off, float (&x)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(P.x) + off));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      h[2 * k] = w[k] & 0xffffu;
-      h[2 * k + 1] = w[k] >> 16;
-    }
+  for (int k = 0; k < 4; ++k) {
+    const uint16_t lo = w[k] & 0xffffu, hi = w[k] >> 16;
+    x[2 * k] = P.bf16 ? __uint_as_float((uint32_t)lo << 16) : __half2float(__ushort_as_half(lo));
+    x[2 * k + 1] = P.bf16 ? __uint_as_float((uint32_t)hi << 16) : __half2float(__ushort_as_half(hi));
   }
-#pragma unroll
-  for (int j = 0; j < VPL; ++j)
-    x[j] = P.bf16 ? __uint_as_float((uint32_t)h[j] << 16) : __half2float(__ushort_as_half(h[j]));
 }
 
+// CTA = one 128-row block of one (sequence, head) of one tensor. A row is
+// spread over LPR = D/8 lanes holding 8 consecutive elements each (16-byte
+// loads, 8-byte stores), so one warp instruction covers 32/LPR rows.
+// Consecutive CTAs take consecutive heads of the same rows, so the CTAs in
+// flight read whole [token, H*D] rows of HBM.
 template <int D>
-__global__ void __launch_bounds__(32 * (D / 16)) fp8_prep_kernel(const PrepBatch pb) {
-  constexpr int NW = D / 16;        // warps per CTA
-  constexpr int RPW = 128 / NW;     // rows per warp
-  constexpr int VPL = D / 32;       // elements per lane per row
-  constexpr int LOG_VPL = VPL == 2 ? 1 : (VPL == 4 ? 2 : 3);
-  constexpr int LOG_D = LOG_VPL + 5;
+__global__ void __launch_bounds__(32 * (D == 256 ? 16 : 8)) fp8_prep_kernel(const PrepBatch pb) {
+  constexpr int NW = D == 256 ? 16 : 8;   // warps per CTA
+  constexpr int LPR = D / 8;               // lanes per row
+  constexpr int RPI = 32 / LPR;            // rows per warp instruction
+  constexpr int RPW = 128 / NW;            // rows per warp
+  constexpr int ITER = RPW / RPI;
+  constexpr int LOG_D = D == 64 ? 6 : (D == 128 ? 7 : 8);
   __shared__ float red[NW];
 
   int bid = blockIdx.x, ti = 0;
@@ -67,57 +57,63 @@ __global__ void __launch_bounds__(32 * (D / 16)) fp8_prep_kernel(const PrepBatch
     ++ti;
   }
   const PrepParams& P = pb.t[ti];
-  const int blk = bid % P.nblk;
-  const int bh = bid / P.nblk;
-  const int h = bh % P.H, b = bh / P.H;
+  const int h = bid % P.H;
+  const int rest = bid / P.H;
+  const int b = rest % P.B;
+  const int blk = rest / P.B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR;              // row of the instruction this lane serves
+  const int d0 = (lane % LPR) * 8;         // first element of the lane
 
-  float sg[VPL];
+  float sg[8];
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) sg[j] = P.sigma ? (float)P.sigma[lane * VPL + j] : 1.f;
+  for (int j = 0; j < 8; ++j) sg[j] = P.sigma ? (float)P.sigma[d0 + j] : 1.f;
   const float norm = P.sigma ? rsqrtf((float)D) : 1.f;
 
-  float x[RPW][VPL];
+  float x[ITER][8];
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < RPW; ++i) {
-    const int row = blk * 128 + warp * RPW + i;
+  for (int i = 0; i < ITER; ++i) {
+    const int row = blk * 128 + warp * RPW + i * RPI + sub;
     if (row < P.S) {
-      load_row<D>(P, (((int64_t)b * P.S + row) * P.H + h) * D + lane * VPL, x[i]);
+      load8(P, (((int64_t)b * P.S + row) * P.H + h) * D + d0, x[i]);
     } else {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) x[i][j] = 0.f;
+      for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
     }
+  }
+#pragma unroll
+  for (int i = 0; i < ITER; ++i) {
     if (P.sigma) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) x[i][j] *= sg[j];
-      // butterflies over the bits of d held inside the lane
+      for (int j = 0; j < 8; ++j) x[i][j] *= sg[j];
+      // Walsh-Hadamard butterflies over the three bits of d inside the lane
 #pragma unroll
-      for (int bit = 0; bit < LOG_VPL; ++bit) {
+      for (int bit = 0; bit < 3; ++bit) {
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
+        for (int j = 0; j < 8; ++j) {
           if (j & (1 << bit)) continue;
           const float a = x[i][j], c = x[i][j | (1 << bit)];
           x[i][j] = a + c;
           x[i][j | (1 << bit)] = a - c;
         }
       }
-      // butterflies over the bits of d that select the lane
+      // ... and over the bits of d that select the lane (within the row's lanes)
 #pragma unroll
-      for (int bit = LOG_VPL; bit < LOG_D; ++bit) {
-        const int m = 1 << (bit - LOG_VPL);
+      for (int bit = 3; bit < LOG_D; ++bit) {
+        const int m = 1 << (bit - 3);
         const bool upper = lane & m;
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
+        for (int j = 0; j < 8; ++j) {
           const float other = __shfl_xor_sync(0xffffffffu, x[i][j], m);
           x[i][j] = upper ? other - x[i][j] : x[i][j] + other;
         }
       }
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) x[i][j] *= norm;
+      for (int j = 0; j < 8; ++j) x[i][j] *= norm;
     }
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
@@ -128,23 +124,17 @@ __global__ void __launch_bounds__(32 * (D / 16)) fp8_prep_kernel(const PrepBatch
   for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax > 0.f ? amax / 448.f : 1.f;
   const float inv = 1.f / scale;
-  if (threadIdx.x == 0) P.scale[(int64_t)bh * P.nblk + blk] = scale;
+  if (threadIdx.x == 0) P.scale[((int64_t)b * P.H + h) * P.nblk + blk] = scale;
 
 #pragma unroll
-  for (int i = 0; i < RPW; ++i) {
-    const int row = blk * 128 + warp * RPW + i;
+  for (int i = 0; i < ITER; ++i) {
+    const int row = blk * 128 + warp * RPW + i * RPI + sub;
     if (row >= P.S) continue;
-    uint8_t* dst = P.x8 + (((int64_t)b * P.S + row) * P.H + h) * D + lane * VPL;
-    uint32_t w[VPL / 2];
+    uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < VPL / 2; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
-    if constexpr (VPL == 2) {
-      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
-    } else if constexpr (VPL == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = w[0] | (w[1] << 16);
-    } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-    }
+    for (int j = 0; j < 4; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
+    *reinterpret_cast<uint2*>(P.x8 + (((int64_t)b * P.S + row) * P.H + h) * D + d0) =
+        make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
   }
 }
 
@@ -160,7 +150,7 @@ cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cud
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffL) return cudaErrorInvalidValue;
   switch (D) {
-    case 64: fp8_prep_kernel<64><<<(unsigned)total, 32 * 4, 0, stream>>>(pb); break;
+    case 64: fp8_prep_kernel<64><<<(unsigned)total, 32 * 8, 0, stream>>>(pb); break;
     case 128: fp8_prep_kernel<128><<<(unsigned)total, 32 * 8, 0, stream>>>(pb); break;
     case 256: fp8_prep_kernel<256><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
     default: return cudaErrorInvalidValue;

@@ -91,13 +91,16 @@ struct FwdCfg {
   static constexpr int kOffKV = QT * kTileBytes;
   static constexpr int kOffBar = kOffKV + STAGES * kTileBytes;
   // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
-  // o_full[2], pv_done, mma_done
+  // o_full[2], pv_done, mma_done, tile_full[R], tile_empty[R]
+  static constexpr int kTileRing = 4;   // work tiles fetched ahead by the load warp
   static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + STAGES,
                        kBarSFull = 2 + 2 * STAGES, kBarPFull = kBarSFull + 2,
                        kBarOFull = kBarPFull + 2, kBarPVDone = kBarOFull + 2,
-                       kBarMmaDone = kBarPVDone + 1, kNumBars = kBarMmaDone + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+                       kBarMmaDone = kBarPVDone + 1, kBarTileFull = kBarMmaDone + 1,
+                       kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
+  static constexpr int kTileConsumers = 1 + kSoftmaxWarps;  // MMA thread + one lane per softmax warp
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem address, abort flag, tile ring
+  static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
 
   static_assert(D == 64 || D == 128 || D == 256, "head dimension");
   static_assert(D % kBoxCols == 0, "a 128-row tile must be whole 128-byte boxes");
@@ -195,10 +198,29 @@ struct Waiter {
   }
 };
 
+// Work-tile hand-off. The load warp fetches tile indices -- the first one is
+// blockIdx.x, later ones come from a global atomic counter so CTAs that drew
+// light tiles (causal, varlen) take more -- and publishes them in a small
+// shared-memory ring; the MMA thread and every softmax warp read the same
+// sequence from it. -1 ends the sequence.
+struct TileRing {
+  uint32_t full0, empty0;   // barrier addresses of slot 0
+  volatile int* slots;
+
+  __device__ __forceinline__ uint32_t full(int s) const { return full0 + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+};
+
+template <int R>
+__device__ __forceinline__ int fetch_tile(const FwdParams& p, int j) {
+  const int w = j == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(p.sched, 1u);
+  return w < p.ntiles ? w : -1;
+}
+
 // ------------------------------------------------------------------ load warp
 template <class C, bool CAUSAL>
 __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                          const FwdParams& p, uint32_t sbase, const Waiter& wt) {
+                          const FwdParams& p, uint32_t sbase, const Waiter& wt, const TileRing& ring) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t kvc = 0, tcount = 0;
@@ -219,7 +241,13 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     return true;
   };
 
-  for (int w = blockIdx.x; ok && w < p.ntiles; w += gridDim.x) {
+  for (int j = 0; ok; ++j) {
+    const int rs = j % C::kTileRing;
+    if (!wt.wait(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 9)) break;
+    const int w = fetch_tile<C::kTileRing>(p, j);
+    ring.slots[rs] = w;
+    ptx::mbar_arrive(ring.full(rs));
+    if (w < 0) break;
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
     if (!wt.wait(bar(C::kBarQEmpty), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
@@ -254,8 +282,23 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
 }
 
 // ------------------------------------------------------------------ MMA warp
+// Next tile from the ring for a consumer; false at the end of the sequence
+// or when the CTA gives up. `lead` lanes arrive on the slot's empty barrier.
+__device__ __forceinline__ bool next_tile(const TileRing& ring, const Waiter& wt, int j, int ring_len,
+                                          bool warp_wide, bool lead, int& w) {
+  const int rs = j % ring_len;
+  const uint32_t par = (j / ring_len) & 1u;
+  const bool ok = warp_wide ? wt.wait_warp(ring.full(rs), par, 10) : wt.wait(ring.full(rs), par, 10);
+  if (!ok) return false;
+  w = ring.slots[rs];
+  if (warp_wide) __syncwarp();
+  if (lead) ptx::mbar_arrive(ring.empty(rs));
+  return w >= 0;
+}
+
 template <class C, bool CAUSAL>
-__device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt) {
+__device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
+                         const TileRing& ring) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   // operand format field: kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = e4m3
@@ -300,7 +343,8 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
 
   uint32_t kvc = 0, it = 0, tcount = 0;
   bool ok = true;
-  for (int w = blockIdx.x; ok && w < p.ntiles; w += gridDim.x) {
+  int w = 0;
+  for (int j = 0; ok && next_tile(ring, wt, j, C::kTileRing, false, true, w); ++j) {
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
     if (!wt.wait(bar(C::kBarQFull), tcount & 1u, 3)) { ok = false; break; }
@@ -391,7 +435,7 @@ __device__ __forceinline__ uint32_t pack_p16(float lo, float hi) {
 
 template <class C, bool CAUSAL>
 __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
-                             int t, int quarter) {
+                             const TileRing& ring, int t, int quarter) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   const int lane = threadIdx.x & 31;
@@ -400,7 +444,8 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
   const float NEG_INF = -CUDART_INF_F;
 
   uint32_t it = 0, tcount = 0;
-  for (int w = blockIdx.x; w < p.ntiles; w += gridDim.x) {
+  int w = 0;
+  for (int jt = 0; next_tile(ring, wt, jt, C::kTileRing, true, lane == 0, w); ++jt) {
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (!ti.live) continue;
     const int row = ti.q0 + 128 * t + r;
@@ -603,8 +648,10 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   if (threadIdx.x == 0) {
     const uint32_t bars = sbase + C::kOffBar;
     for (int i = 0; i < C::kNumBars; ++i) {
-      const bool is_pfull = i == C::kBarPFull || i == C::kBarPFull + 1;
-      ptx::mbar_init(bars + 8u * i, is_pfull ? 4u : 1u);
+      uint32_t count = 1;
+      if (i == C::kBarPFull || i == C::kBarPFull + 1) count = 4;
+      if (i >= C::kBarTileEmpty) count = C::kTileConsumers;
+      ptx::mbar_init(bars + 8u * i, count);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -623,18 +670,20 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const Waiter wt{abort_flag, p.status};
+  const TileRing ring{sbase + C::kOffBar + 8u * C::kBarTileFull, sbase + C::kOffBar + 8u * C::kBarTileEmpty,
+                      reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
   // each role runs inside the branch that set its register budget, so the
   // register allocator sees one budget per role
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kRebalance) ptx::setmaxnreg_dec<C::kRegsLow>();
     if (warp == C::kLoadWarp) {
-      if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt);
+      if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
     } else if (warp == C::kMmaWarp) {
-      if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt);
+      if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt, ring);
     }
   } else {
     if constexpr (C::kRebalance) ptx::setmaxnreg_inc<C::kRegsHigh>();
-    softmax_role<C, CAUSAL>(p, sbase, tmem, wt, warp >> 2, warp & 3);
+    softmax_role<C, CAUSAL>(p, sbase, tmem, wt, ring, warp >> 2, warp & 3);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -642,6 +691,14 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   if (warp == C::kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // every fetch of this CTA is done; the last CTA out re-arms the counter
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
   }
 }
 
