@@ -51,6 +51,10 @@ def lib():
         L.fa_fp8_prep.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
         L.fa_fwd_fp8.restype = i
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+        L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.fa_fwd_splitkv.restype = i
+        L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, i, vp]
         L.fa_get_device_status.restype = i
         L.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i)]
         L.fa_strerror.restype = ctypes.c_char_p
@@ -91,6 +95,44 @@ def fa_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q=None, c
     if check and st != FA_OK:
         raise FAError(st, "fa_fwd")
     return st
+
+
+def fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_size(int(B), int(H), int(Sq), int(Sk), int(D), int(num_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, num_splits, workspace, workspace_bytes,
+                   dtype=None, stream=None, check=True) -> int:
+    """Raw entry point: split-KV forward with a caller-owned workspace."""
+    if dtype is None:
+        dtype = _DTYPE[q.dtype]
+    st = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(Sq), int(Sk),
+                              int(D), float(scale), int(bool(causal)), int(num_splits), _ptr(workspace),
+                              int(workspace_bytes), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv")
+    return st
+
+
+def attention_forward_splitkv(q, k, v, *, batch, causal=False, scale=None, num_splits=0, workspace=None,
+                              out=None, lse=None, stream=None):
+    """Allocate O, LSE and (unless given) the workspace with torch and call
+    ``fa_fwd_splitkv``. q ``[B*Sq, H, D]``, k/v ``[B*Sk, H, D]``."""
+    B = batch
+    H, D = q.shape[1], q.shape[2]
+    Sq, Sk = q.shape[0] // B, k.shape[0] // B
+    if scale is None:
+        scale = D ** -0.5
+    nbytes = fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), device=q.device, dtype=torch.float32)
+    fa_fwd_splitkv(q, k, v, out, lse, B, H, Sq, Sk, D, scale, causal, num_splits, workspace,
+                   workspace.numel() * workspace.element_size(), stream=stream)
+    return out, lse
 
 
 def fa_fp8_prep(q, k, v, q8, k8, v8, q_scale, k_scale, v_scale, sigma, B, H, Sq, Sk, D, in_dtype=None,

@@ -26,6 +26,7 @@ __device__ unsigned int g_fa_sched[kSchedSlots][2];
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 256;   // key ranges of the split-KV forward, at most
 
 struct DevInfo {
   bool ready = false;
@@ -130,9 +131,18 @@ const char* fa_strerror(int s) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
-           int Sk, int D, float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
-           int total_q, int total_k, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks and launch description shared by the 16-bit entry points
+// (everything but the split-KV fields). Returns FA_OK, or the status to
+// report; `nothing` is set when the problem is empty.
+int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, const void* k,
+                const void* v, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
+                int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, int total_q, int total_k,
+                int dtype, void* stream) {
+  *nothing = false;
   // ---- host-side argument checks (no device access)
   if (dtype == FA_FP8_E4M3) return FA_ERR_UNSUPPORTED;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
@@ -147,7 +157,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const int64_t Tk = varlen ? total_k : (int64_t)B * Sk;
   if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
   if ((int64_t)H * D * 2 > (int64_t)1 << 38) return FA_ERR_INVALID_ARG;
-  if (B == 0 || Tq == 0 || Sq == 0) return FA_OK;  // nothing to compute
+  if (B == 0 || Tq == 0 || Sq == 0) {  // nothing to compute
+    *nothing = true;
+    return FA_OK;
+  }
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -161,8 +174,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   DevInfo* dev = nullptr;
   int st = current_device(&dev);
   if (st != FA_OK) return st;
+  *devp = dev;
 
-  fa::FwdLaunch L;
   std::memset(&L, 0, sizeof(L));
   const CUtensorMapDataType dt = dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -184,19 +197,110 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   L.p.ntiles = (int)ntiles;
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
-  L.p.sched = dev->take_slot();
+  L.p.n_split = 1;
+  L.p.split_blocks = 1 << 30;
   L.D = D;
   L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
   L.causal = causal != 0;
   L.num_sms = dev->sms;
   L.stream = static_cast<cudaStream_t>(stream);
+  return FA_OK;
+}
 
+int launch16(fa::FwdLaunch& L, DevInfo* dev) {
+  L.p.sched = dev->take_slot();
   cudaError_t e;
-  switch (D) {
+  switch (L.D) {
     case 64: e = fa::launch_fwd_d64(L); break;
     case 128: e = fa::launch_fwd_d128(L); break;
     default: e = fa::launch_fwd_d256(L); break;
   }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+// Key ranges of the split-KV forward: `requested` <= 0 picks enough ranges for
+// about two work tiles per SM. Returns the ranges actually used (every range
+// non-empty) and their length in 128-key blocks.
+void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms, int* n_split,
+                    int* split_blocks) {
+  const int64_t nblocks = ((int64_t)Sk + 127) / 128;
+  const int rows = fa::cta_rows(D);
+  const int64_t tiles = (int64_t)B * H * (((int64_t)Sq + rows - 1) / rows);
+  int64_t n = requested;
+  if (n <= 0) n = tiles > 0 ? (2 * (int64_t)sms + tiles - 1) / tiles : 1;
+  if (n > kMaxSplits) n = kMaxSplits;
+  if (n > nblocks) n = nblocks;
+  if (n < 1) n = 1;
+  const int64_t per = (nblocks + n - 1) / n;
+  *split_blocks = (int)(per < 1 ? 1 : per);
+  *n_split = (int)(per < 1 ? 1 : (nblocks + per - 1) / per);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the split-KV forward: partial O (fp32) then partial LSE.
+size_t splitkv_bytes(int B, int H, int Sq, int D, int n_split) {
+  return round256((size_t)n_split * B * Sq * H * D * sizeof(float)) + (size_t)n_split * B * H * Sq * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+           int Sk, int D, float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+           int total_q, int total_k, int dtype, void* stream) {
+  fa::FwdLaunch L;
+  DevInfo* dev = nullptr;
+  bool nothing = false;
+  int st = setup_fwd16(L, &dev, &nothing, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q,
+                       cu_seqlens_k, total_q, total_k, dtype, stream);
+  if (st != FA_OK || nothing) return st;
+  return launch16(L, dev);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Sq, int Sk, int D, int num_splits) {
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk < 0 || (D != 64 && D != 128 && D != 256)) return 0;
+  int sms = 0;
+  if (num_splits <= 0) {
+    DevInfo* dev = nullptr;
+    if (current_device(&dev) != FA_OK) return 0;
+    sms = dev->sms;
+  }
+  int n = 1, per = 1;
+  resolve_splits(B, H, Sq, Sk, D, num_splits, sms, &n, &per);
+  return splitkv_bytes(B, H, Sq, D, n);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                   int Sk, int D, float scale, int causal, int num_splits, void* workspace,
+                   size_t workspace_bytes, int dtype, void* stream) {
+  fa::FwdLaunch L;
+  DevInfo* dev = nullptr;
+  bool nothing = false;
+  int st = setup_fwd16(L, &dev, &nothing, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, nullptr, nullptr,
+                       0, 0, dtype, stream);
+  if (st != FA_OK || nothing) return st;
+  int n = 1, per = 1;
+  resolve_splits(B, H, Sq, Sk, D, num_splits, dev->sms, &n, &per);
+  const size_t need = splitkv_bytes(B, H, Sq, D, n);
+  if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  const int64_t ntiles = (int64_t)L.p.ntiles * n;
+  if (ntiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  L.p.ntiles = (int)ntiles;
+  L.p.n_split = n;
+  L.p.split_blocks = per;
+  L.p.o_part = static_cast<float*>(workspace);
+  L.p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          round256((size_t)n * B * Sq * H * D * sizeof(float)));
+  if ((st = launch16(L, dev)) != FA_OK) return st;
+  cudaError_t e = fa::launch_splitkv_merge(L.p.o_part, L.p.lse_part, o, lse, n, B, H, Sq, D,
+                                           dtype == FA_FP16, L.stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -298,6 +402,8 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_sc
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
   L.p.sched = dev->take_slot();
+  L.p.n_split = 1;
+  L.p.split_blocks = 1 << 30;
   L.p.q_scale = q_scale;
   L.p.k_scale = k_scale;
   L.p.v_scale = v_scale;

@@ -36,6 +36,14 @@ struct FwdParams {
   const float* k_scale;
   const float* v_scale;
   int nblk_q, nblk_k;
+  // split-KV: the keys of every (sequence, head) are cut into n_split ranges
+  // of split_blocks 128-key blocks; each work tile covers one range and writes
+  // a partial, self-normalised fp32 O and its LSE into o_part / lse_part
+  // ([n_split, tokens_q, H, D] and [n_split, B, H, Sq]). n_split = 1 and
+  // o_part = nullptr: no split, O and LSE are written directly.
+  int n_split, split_blocks;
+  float* o_part;
+  float* lse_part;
 };
 
 // Element kinds of the attention inputs.
@@ -58,6 +66,8 @@ constexpr int cta_rows(int D) { return D <= 128 ? 256 : 128; }
 cudaError_t launch_fwd_d64(const FwdLaunch& L);
 cudaError_t launch_fwd_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_d256(const FwdLaunch& L);
+cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                                 int n_split, int B, int H, int Sq, int D, int out_fp16, cudaStream_t stream);
 cudaError_t launch_fwd_fp8_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
 

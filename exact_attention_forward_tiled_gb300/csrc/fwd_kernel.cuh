@@ -111,6 +111,8 @@ struct FwdCfg {
 // Work tile: CTA query block of one (sequence, head).
 struct TileInfo {
   int b, h;
+  int split;       // key range (split-KV) of this tile, 0 without split
+  int kb0;         // first 128-key block of the range
   int qblk;        // CTA query block index within the sequence
   int q0;          // first query row of the block within its sequence
   int Lq, Lk;      // sequence lengths
@@ -125,8 +127,11 @@ struct TileInfo {
 template <int ROWS, bool CAUSAL>
 __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   TileInfo t;
-  const int bh = w / p.n_qblk;
-  const int j = w - bh * p.n_qblk;
+  const int per_head = p.n_qblk * p.n_split;
+  const int bh = w / per_head;
+  const int jj = w - bh * per_head;
+  const int j = jj / p.n_split;
+  t.split = jj - j * p.n_split;
   const int qblk = CAUSAL ? (p.n_qblk - 1 - j) : j;
   t.qblk = qblk;
   t.b = bh / p.H;
@@ -153,12 +158,14 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   }
   t.q0 = qblk * ROWS;
   t.live = t.q0 < t.Lq;
+  t.kb0 = t.split * p.split_blocks;
   int n = 0;
   if (t.live) {
     const int last = min(t.q0 + ROWS, t.Lq) - 1;
     int lim = t.Lk;
     if (CAUSAL) lim = min(lim, last + t.Lk - t.Lq + 1);
-    n = lim > 0 ? (lim + 127) / 128 : 0;
+    const int kb1 = min(lim > 0 ? (lim + 127) / 128 : 0, t.kb0 + p.split_blocks);
+    n = max(kb1 - t.kb0, 0);
   }
   t.n_kv = n;
   return t;
@@ -258,17 +265,18 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
                 bar(C::kBarQFull));
     ++tcount;
     const int n = ti.n_kv;
+    const int krow = ti.ktok + 128 * ti.kb0;   // first key row of the tile's range
     if (C::QT == 2) {
       // consumption order of the MMA warp: K0, V0, K1, V1, ...
       for (int i = 0; ok && i < n; ++i) {
-        ok = load_kv(tk, ti.h, ti.ktok + 128 * i) && load_kv(tv, ti.h, ti.ktok + 128 * i);
+        ok = load_kv(tk, ti.h, krow + 128 * i) && load_kv(tv, ti.h, krow + 128 * i);
       }
     } else {
       // consumption order: K0, K1, V0, K2, V1, ..., V_{n-1}
-      ok = load_kv(tk, ti.h, ti.ktok);
+      ok = load_kv(tk, ti.h, krow);
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n) ok = load_kv(tk, ti.h, ti.ktok + 128 * (i + 1));
-        if (ok) ok = load_kv(tv, ti.h, ti.ktok + 128 * i);
+        if (i + 1 < n) ok = load_kv(tk, ti.h, krow + 128 * (i + 1));
+        if (ok) ok = load_kv(tv, ti.h, krow + 128 * i);
       }
     }
   }
@@ -451,14 +459,21 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     const int row = ti.q0 + 128 * t + r;
     const bool row_ok = row < ti.Lq;
     const int64_t tok = (int64_t)ti.qtok + row;
+    const bool split = p.o_part != nullptr;
     uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + ti.h) * C::D;
-    float* lse_ptr = p.cu_q != nullptr
-                         ? p.lse + (int64_t)ti.h * p.total_q + tok
-                         : p.lse + ((int64_t)ti.b * p.H + ti.h) * p.Sq + row;
+    float* oprow = split ? p.o_part + (((int64_t)ti.split * p.total_q + tok) * p.H + ti.h) * C::D : nullptr;
+    float* lse_ptr = split ? p.lse_part + (((int64_t)ti.split * p.B + ti.b) * p.H + ti.h) * p.Sq + row
+                     : p.cu_q != nullptr ? p.lse + (int64_t)ti.h * p.total_q + tok
+                                         : p.lse + ((int64_t)ti.b * p.H + ti.h) * p.Sq + row;
     if (ti.n_kv == 0) {
-      // no visible key for any row of this block: O = 0, LSE = -inf
+      // no visible key for any row of this block (or of this key range):
+      // O = 0, LSE = -inf
       if (row_ok) {
-        for (int d = 0; d < C::D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        if (split) {
+          for (int d = 0; d < C::D; d += 4) *reinterpret_cast<float4*>(oprow + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          for (int d = 0; d < C::D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        }
         *lse_ptr = NEG_INF;
       }
       continue;
@@ -481,9 +496,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     float m_ref = NEG_INF, l = 0.f;
     bool ok = true;
     for (int i = 0; i < ti.n_kv; ++i, ++it) {
-      const float c = C::kFp8 ? c_q * __ldg(ks_row + i) : c_q;
+      const int kb = ti.kb0 + i;   // absolute 128-key block
+      const float c = C::kFp8 ? c_q * __ldg(ks_row + kb) : c_q;
       // log2 of the factor the stored P carries: 2^kappa * v_s(j) / v_ref (e4m3 only)
-      const float lg_pw = C::kFp8 ? ptx::lg2(__ldg(vs_row + i) * inv_vref) + C::kLog2Kappa : 0.f;
+      const float lg_pw = C::kFp8 ? ptx::lg2(__ldg(vs_row + kb) * inv_vref) + C::kLog2Kappa : 0.f;
       const int buf = C::QT == 2 ? t : (int)(it & 1u);
       const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
       if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;
@@ -499,7 +515,7 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
       float s[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(sv[j]);
-      const int lim_local = key_lim - 128 * i;
+      const int lim_local = key_lim - 128 * kb;
       const bool masked = lim_local < 128;  // keys j >= lim_local are not visible
       if (masked) {
 #pragma unroll
@@ -615,6 +631,17 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
       ptx::tmem_ld32(o_addr + 32 * ch, v);
       ptx::tmem_wait_ld();
       ptx::reg_fence(v);
+      if (split) {
+        // partial O of this key range, fp32, normalised by its own l
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(oprow + 32 * ch);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                 __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
+        }
+        continue;
+      }
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)

@@ -30,6 +30,7 @@ class Workload:
     varlen: bool = False
     len_range: tuple = (128, 8192)   # varlen: inclusive uniform range of lengths
     outliers: bool = False           # fp8 outlier workload
+    splitkv: bool = False            # run through the split-KV forward
     note: str = field(default="", compare=False)
 
 
@@ -48,6 +49,10 @@ WORKLOADS = {
                    outliers=True,
                    note="fp8 e4m3 B=4 H=16 Sq=Sk=8192 D=128 non-causal, block scales + Hadamard, "
                         "0.1% N(0,10^2) outliers in 4 fixed columns"),
+    # split-KV: few query rows against a long key sequence, where B*H*ceil(Sq/256)
+    # = 16 work tiles alone would leave most SMs idle
+    "f1": Workload("bf16_splitkv_B2_H8_Sq256_Sk65536_D128", "bf16", 2, 8, 256, 65536, 128, False, 6,
+                   splitkv=True, note="bf16 split-KV B=2 H=8 Sq=256 Sk=65536 D=128 non-causal"),
 }
 
 TORCH_DTYPE = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.bfloat16}

@@ -26,11 +26,14 @@
  *     by the return value, errors found on the device by
  *     fa_get_device_status().
  *   - Return value: FA_OK (0) or a negative FA_ERR_* code (fa_strerror()).
- *   - The library allocates no memory per call. Its only device state is one
- *     status word per device (a static __device__ variable).
+ *   - The library allocates no memory. Its only device state is a status
+ *     word and a small set of tile-scheduler counters per device (static
+ *     __device__ variables); scratch that a call needs is passed in.
  */
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -76,6 +79,34 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Sq, int Sk, int D, float scale, int causal,
            const int* cu_seqlens_q, const int* cu_seqlens_k, int total_q, int total_k,
            int dtype, void* stream);
+
+/*
+ * fa_fwd_splitkv -- the same forward with the keys of every (sequence, head)
+ * cut into ranges that run as separate work tiles, then merged: each range r
+ * gives a self-normalised partial O_r and LSE_r, and the rows over all keys
+ * are LSE = ln sum_r exp(LSE_r), O = sum_r exp(LSE_r - LSE) O_r (the partial
+ * softmax of FlashDecoding, in the lineage of the "FlashAttention-3
+ * (lukebest wiki)" page). It fills the GPU when B * H * ceil(Sq/256) work
+ * tiles alone would not (short Sq, long Sk).
+ *
+ *   arguments as fa_fwd, fixed length only (no cu_seqlens)
+ *   num_splits   key ranges; <= 0 picks about two work tiles per SM. It is
+ *                capped at 256 and at ceil(Sk/128), and trimmed so that no
+ *                range is empty.
+ *   workspace    device scratch of at least
+ *                fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits)
+ *                bytes, 256-byte aligned, owned by the caller; its contents
+ *                on entry do not matter and are overwritten (partial O in
+ *                fp32, then partial LSE). Calls that share a workspace and
+ *                overlap on the GPU race.
+ *
+ * Returns FA_ERR_INVALID_ARG if the workspace is missing or too small.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Sq, int Sk, int D, int num_splits);
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                   int num_splits, void* workspace, size_t workspace_bytes, int dtype,
+                   void* stream);
 
 /*
  * fa_fp8_prep -- FP8 preparation of the inputs ("FlashAttention-3 (lukebest

@@ -208,6 +208,26 @@ def attention_rows(q, k, v, rows, *, scale, causal, nseq, Sq=None, Sk=None,
     return o, lse
 
 
+def merge_partials(o_parts, lse_parts):
+    """Combine attention over disjoint key ranges into attention over their
+    union: LSE = ln sum_r exp(LSE_r), O = sum_r exp(LSE_r - LSE) O_r, where
+    O_r is normalised over range r alone (the partial softmax of
+    FlashDecoding, named in the "FlashAttention-3 (lukebest wiki)" lineage).
+    o_parts [R, n, D], lse_parts [R, n]; a range with LSE_r = -inf carries no
+    weight, and a row with no visible key at all gets O = 0, LSE = -inf."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    o = np.zeros(o_parts.shape[1:])
+    lse = np.full(lse_parts.shape[1:], -np.inf)
+    ok = np.isfinite(m)
+    w = np.where(np.isfinite(lse_parts), np.exp(lse_parts - np.where(ok, m, 0.0)), 0.0)
+    tot = w.sum(axis=0)
+    o[ok] = (w[:, ok, None] * o_parts[:, ok]).sum(axis=0) / tot[ok, None]
+    lse[ok] = m[ok] + np.log(tot[ok])
+    return o, lse
+
+
 def visible_pairs(qpos, Lk, Lq, causal) -> int:
     """Number of (row, visible key) pairs of the given rows."""
     qpos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))

@@ -98,3 +98,28 @@ def test_pages_numbers():
     t = g["h100_fp16_matmul_vs_mufu_tflops"]
     ratio = (t["matmul"] / t["mufu"]) / e["value"]
     assert abs(ratio - g["exp_time_fraction_of_matmul"]["value"]) < 0.01
+
+
+@pytest.mark.parametrize("cuts", [[0, 40], [0, 1, 2, 97], [0, 30, 31, 60, 120]])
+def test_merge_of_key_ranges_equals_full(cuts):
+    """Attention over disjoint key ranges, merged, is attention over all keys
+    (the identity split-KV relies on); pinned against the direct definition."""
+    r = np.random.default_rng(len(cuts))
+    Lq, Lk, D = 17, 120, 32
+    q, k, v = r.standard_normal((Lq, D)), r.standard_normal((Lk, D)), r.standard_normal((Lk, D))
+    edges = cuts + [Lk]
+    parts = [O.attention_head(q, np.arange(Lq), k[a:b], v[a:b], Lq, 0.3, False)
+             for a, b in zip(edges[:-1], edges[1:])]
+    o, lse = O.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+    o_ref, lse_ref = O.attention_head(q, np.arange(Lq), k, v, Lq, 0.3, False)
+    assert np.abs(o - o_ref).max() < 1e-12 and np.abs(lse - lse_ref).max() < 1e-12
+
+
+def test_merge_handles_empty_ranges():
+    o1 = np.array([[1.0, 2.0], [0.0, 0.0]])
+    l1 = np.array([0.5, -np.inf])
+    o2 = np.zeros((2, 2))
+    l2 = np.array([-np.inf, -np.inf])
+    o, lse = O.merge_partials([o1, o2], [l1, l2])
+    assert np.array_equal(o[0], o1[0]) and lse[0] == 0.5
+    assert np.all(o[1] == 0) and lse[1] == -np.inf
