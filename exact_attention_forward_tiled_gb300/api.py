@@ -114,6 +114,24 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, num_splits, 
     return st
 
 
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, num_splits, dtype=None,
+                           stream=None, check=True) -> int:
+    """Raw entry point: split-KV forward whose scratch is the library's own
+    fixed array, for callers that cannot allocate device memory."""
+    L = lib()
+    fn = L.fa_fwd_splitkv_noalloc
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    fn.restype = i
+    fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, i, vp]
+    if dtype is None:
+        dtype = _DTYPE[q.dtype]
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(Sq), int(Sk), int(D), float(scale),
+            int(bool(causal)), int(num_splits), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv_noalloc")
+    return st
+
+
 def attention_forward_splitkv(q, k, v, *, batch, causal=False, scale=None, num_splits=0, workspace=None,
                               out=None, lse=None, stream=None):
     """Allocate O, LSE and (unless given) the workspace with torch and call

@@ -127,6 +127,7 @@ const char* fa_strerror(int s) {
     case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out; outputs incomplete";
     case FA_ERR_DEVICE_SEQLENS: return "cu_seqlens entry out of bounds; sequence skipped";
     case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in 64 MiB array holds";
     default: return "unknown status";
   }
 }

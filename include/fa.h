@@ -47,6 +47,7 @@ extern "C" {
 #define FA_ERR_DEVICE_TIMEOUT -5  /* a kernel wait gave up (see status)        */
 #define FA_ERR_DEVICE_SEQLENS -6  /* a cu_seqlens entry broke its bounds       */
 #define FA_ERR_NO_DEVICE -7       /* no sm_100-family device is current        */
+#define FA_ERR_SCRATCH_LIMIT -8   /* needs more than the built-in scratch      */
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
 
@@ -107,6 +108,28 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int B, int H, int Sq, int Sk, int D, float scale, int causal,
                    int num_splits, void* workspace, size_t workspace_bytes, int dtype,
                    void* stream);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory (no cudaMalloc where they run, or an allocator that must not
+ * grow). It takes no workspace: the scratch is a fixed 64 MiB array inside
+ * the library, present on every device that loads the library until the
+ * process exits. The pages have no counterpart of this entry point.
+ *
+ *   arguments as fa_fwd_splitkv, without workspace and workspace_bytes
+ *
+ * Returns FA_ERR_SCRATCH_LIMIT, before touching any pointer, when
+ * fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits) exceeds 64 MiB
+ * (ask for fewer key ranges, or use fa_fwd_splitkv). The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture. All calls share the one array:
+ * calls that overlap on the GPU (other streams, other threads) race and give
+ * wrong results. Nothing in it needs clearing between calls: every byte a
+ * call reads, the same call has written. Allocates nothing.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                           int num_splits, int dtype, void* stream);
 
 /*
  * fa_fp8_prep -- FP8 preparation of the inputs ("FlashAttention-3 (lukebest
