@@ -42,8 +42,8 @@ __device__ __forceinline__ void load8(const PrepParams& P, int64_t off, float (&
 // Consecutive CTAs take consecutive heads of the same rows, so the CTAs in
 // flight read whole [token, H*D] rows of HBM.
 template <int D>
-__global__ void __launch_bounds__(32 * (D == 256 ? 16 : 8)) fp8_prep_kernel(const PrepBatch pb) {
-  constexpr int NW = D == 256 ? 16 : 8;   // warps per CTA
+__global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) fp8_prep_kernel(const PrepBatch pb) {
+  constexpr int NW = D == 256 ? 32 : 16;  // warps per CTA (4 loads in flight per lane)
   constexpr int LPR = D / 8;               // lanes per row
   constexpr int RPI = 32 / LPR;            // rows per warp instruction
   constexpr int RPW = 128 / NW;            // rows per warp
@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 16 : 8)) fp8_prep_kernel(cons
   float sg[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) sg[j] = P.sigma ? (float)P.sigma[d0 + j] : 1.f;
+  // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
   const float norm = P.sigma ? rsqrtf((float)D) : 1.f;
 
   float x[ITER][8];
@@ -98,19 +99,19 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 16 : 8)) fp8_prep_kernel(cons
           x[i][j | (1 << bit)] = a - c;
         }
       }
-      // ... and over the bits of d that select the lane (within the row's lanes)
+      // ... and over the bits of d that select the lane (within the row's
+      // lanes): lower partner a + b, upper partner a - b = other - mine, one
+      // FFMA each with the sign of the lane's half
 #pragma unroll
       for (int bit = 3; bit < LOG_D; ++bit) {
         const int m = 1 << (bit - 3);
-        const bool upper = lane & m;
+        const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float other = __shfl_xor_sync(0xffffffffu, x[i][j], m);
-          x[i][j] = upper ? other - x[i][j] : x[i][j] + other;
+          x[i][j] = fmaf(x[i][j], sgn, other);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[i][j] *= norm;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
@@ -122,8 +123,9 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 16 : 8)) fp8_prep_kernel(cons
   amax = red[0];
 #pragma unroll
   for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
+  amax *= norm;   // amax of the rotated, normalised values
   const float scale = amax > 0.f ? amax / 448.f : 1.f;
-  const float inv = 1.f / scale;
+  const float inv = norm / scale;
   if (threadIdx.x == 0) P.scale[((int64_t)b * P.H + h) * P.nblk + blk] = scale;
 
 #pragma unroll
@@ -150,9 +152,9 @@ cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cud
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffL) return cudaErrorInvalidValue;
   switch (D) {
-    case 64: fp8_prep_kernel<64><<<(unsigned)total, 32 * 8, 0, stream>>>(pb); break;
-    case 128: fp8_prep_kernel<128><<<(unsigned)total, 32 * 8, 0, stream>>>(pb); break;
-    case 256: fp8_prep_kernel<256><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
+    case 64: fp8_prep_kernel<64><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
+    case 128: fp8_prep_kernel<128><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
+    case 256: fp8_prep_kernel<256><<<(unsigned)total, 32 * 32, 0, stream>>>(pb); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
