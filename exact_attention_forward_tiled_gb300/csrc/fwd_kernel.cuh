@@ -70,6 +70,10 @@ struct FwdCfg {
   // lazy-rescale threshold (log2 units) and, for e4m3, the power of two P is
   // scaled by before it is rounded (P * 2^kappa <= 2^(tau + kappa) = 256 < 448)
   static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
+  // P handed to the MMA warp in two halves of 64 keys (e4m3, where the MMAs
+  // are short and the softmax is the critical path) or in one piece (16-bit,
+  // where the extra store round trip costs more than it saves)
+  static constexpr bool kSplitP = kFp8;
   static constexpr float kKappaScale = kFp8 ? 16.0f : 1.0f;
   static constexpr float kLog2Kappa = kFp8 ? 4.0f : 0.0f;
   static constexpr int kSoftmaxWarps = 4 * QT;
@@ -90,12 +94,13 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = QT * kTileBytes;
   static constexpr int kOffBar = kOffKV + STAGES * kTileBytes;
-  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2],
+  // p_full[2][2] (per score buffer, first / second half of the keys),
   // o_full[2], pv_done, mma_done, tile_full[R], tile_empty[R]
   static constexpr int kTileRing = 4;   // work tiles fetched ahead by the load warp
   static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + STAGES,
                        kBarSFull = 2 + 2 * STAGES, kBarPFull = kBarSFull + 2,
-                       kBarOFull = kBarPFull + 2, kBarPVDone = kBarOFull + 2,
+                       kBarOFull = kBarPFull + 4, kBarPVDone = kBarOFull + 2,
                        kBarMmaDone = kBarPVDone + 1, kBarTileFull = kBarMmaDone + 1,
                        kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
   static constexpr int kTileConsumers = 1 + kSoftmaxWarps;  // MMA thread + one lane per softmax warp
@@ -330,10 +335,16 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         ptx::mma_f16_ss(tmem + s_col, a, b, idesc_qk, kk > 0);
     }
   };
-  // O[o_col] (+)= P[p_col] V : steps of kKeysPerStep keys; 8 P columns per step
-  auto pv = [&](uint32_t o_col, uint32_t p_col, uint32_t v_addr, bool acc) {
+  // O[o_col] (+)= P[p_col] V : steps of kKeysPerStep keys; 8 P columns per
+  // step. P arrives in two halves (keys 0-63, 64-127), each with its own
+  // barrier, so the first half's MMAs start while the second half is made.
+  auto pv = [&](uint32_t o_col, uint32_t p_col, uint32_t v_addr, bool acc, int pbuf, uint32_t parity) -> bool {
 #pragma unroll
     for (int kk = 0; kk < C::kPvSteps; ++kk) {
+      if (kk == 0 || (C::kSplitP && kk == C::kPvSteps / 2)) {
+        if (!wt.wait(bar(C::kBarPFull + 2 * pbuf + (kk == 0 ? 0 : 1)), parity, 5)) return false;
+        ptx::tc_fence_after();
+      }
       const uint64_t b =
           ptx::smem_desc_sw128(v_addr + kk * C::kKeysPerStep * 128, C::kBoxBytes, 1024);
       const uint32_t en = (acc || kk > 0) ? 1u : 0u;
@@ -342,6 +353,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
       else
         ptx::mma_f16_ts(tmem + o_col, tmem + p_col + kk * 8, b, idesc_pv, en);
     }
+    return true;
   };
   auto kv_ready = [&](uint32_t c) {
     const bool r = wt.wait(bar(C::kBarKVFull + slot(c)), (c / C::STAGES) & 1u, 4);
@@ -366,9 +378,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
       for (int i = 0; i < n; ++i) {
         const uint32_t ck = kvc + 2 * i, cv = ck + 1;
         if (i > 0) {
-          if (!(ok = wt.wait(bar(C::kBarPFull + 1), (it + i - 1) & 1u, 5))) break;
-          ptx::tc_fence_after();
-          pv(C::col_o(1), C::col_s(1), slot_addr(cv - 2), i - 1 > 0);
+          if (!(ok = pv(C::col_o(1), C::col_s(1), slot_addr(cv - 2), i - 1 > 0, 1, (it + i - 1) & 1u))) break;
           ptx::mma_commit(bar(C::kBarKVEmpty + slot(cv - 2)));
         }
         qk(C::col_s(1), sq + C::kTileBytes, slot_addr(ck));
@@ -376,9 +386,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         ptx::mma_commit(bar(C::kBarKVEmpty + slot(ck)));
         if (i == n - 1) ptx::mma_commit(bar(C::kBarQEmpty));
         if (!(ok = kv_ready(cv))) break;
-        if (!(ok = wt.wait(bar(C::kBarPFull + 0), (it + i) & 1u, 5))) break;
-        ptx::tc_fence_after();
-        pv(C::col_o(0), C::col_s(0), slot_addr(cv), i > 0);
+        if (!(ok = pv(C::col_o(0), C::col_s(0), slot_addr(cv), i > 0, 0, (it + i) & 1u))) break;
         if (i == n - 1) ptx::mma_commit(bar(C::kBarOFull + 0));
         if (i + 1 < n) {
           if (!(ok = kv_ready(ck + 2))) break;
@@ -387,10 +395,8 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         }
       }
       if (!ok) break;
-      if (!(ok = wt.wait(bar(C::kBarPFull + 1), (it + n - 1) & 1u, 5))) break;
-      ptx::tc_fence_after();
       const uint32_t cl = kvc + 2 * n - 1;
-      pv(C::col_o(1), C::col_s(1), slot_addr(cl), n - 1 > 0);
+      if (!(ok = pv(C::col_o(1), C::col_s(1), slot_addr(cl), n - 1 > 0, 1, (it + n - 1) & 1u))) break;
       ptx::mma_commit(bar(C::kBarKVEmpty + slot(cl)));
       ptx::mma_commit(bar(C::kBarOFull + 1));
       kvc += 2 * n;
@@ -413,9 +419,8 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
           if (i + 1 == n - 1) ptx::mma_commit(bar(C::kBarQEmpty));
         }
         if (!(ok = kv_ready(kvc))) break;
-        if (!(ok = wt.wait(bar(C::kBarPFull + (int)(iti & 1u)), (iti >> 1) & 1u, 5))) break;
-        ptx::tc_fence_after();
-        pv(C::col_o(0), C::col_s(iti & 1u), slot_addr(kvc), i > 0);
+        if (!(ok = pv(C::col_o(0), C::col_s(iti & 1u), slot_addr(kvc), i > 0, (int)(iti & 1u), (iti >> 1) & 1u)))
+          break;
         ptx::mma_commit(bar(C::kBarKVEmpty + slot(kvc)));
         ptx::mma_commit(bar(C::kBarPVDone));
         ++kvc;
@@ -566,21 +571,46 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
           ptx::tmem_wait_st();
         }
       }
-      // exponent argument s * c - m (+ log2 of the e4m3 P weight), two lanes at a time
+      // exponent argument s * c - m (+ log2 of the e4m3 P weight), two lanes
+      // at a time; P goes out in two halves of 64 keys, each released to the
+      // MMA warp as soon as it sits in tensor memory; the row sum comes after
       const float mu = (m_ref == NEG_INF ? 0.f : m_ref) - lg_pw;
       const uint64_t c2 = ptx::f2pack(c, c), nm2 = ptx::f2pack(-mu, -mu);
 #pragma unroll
-      for (int j = 0; j < 128; j += 2) {
-        float lo, hi;
-        ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
-        s[j] = ptx::ex2(lo);
-        s[j + 1] = ptx::ex2(hi);
-      }
-      if (masked) {
-        // zero the invisible keys after the exponent: with c = 0 their
-        // -inf * c would be NaN
+      for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) s[j] = j < lim_local ? s[j] : 0.f;
+        for (int j = 64 * hf; j < 64 * hf + 64; j += 2) {
+          float lo, hi;
+          ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
+          s[j] = ptx::ex2(lo);
+          s[j + 1] = ptx::ex2(hi);
+        }
+        if (masked) {
+          // zero the invisible keys after the exponent: with c = 0 their
+          // -inf * c would be NaN
+#pragma unroll
+          for (int j = 64 * hf; j < 64 * hf + 64; ++j) s[j] = j < lim_local ? s[j] : 0.f;
+        }
+        if (C::kFp8) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int e = 64 * hf + 4 * j;
+            pk[j] = ptx::pack_e4m3x2(s[e], s[e + 1]) | (ptx::pack_e4m3x2(s[e + 2], s[e + 3]) << 16);
+          }
+          ptx::tmem_st16(s_addr + 16 * hf, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[64 * hf + 2 * j], s[64 * hf + 2 * j + 1]);
+          ptx::tmem_st32(s_addr + 32 * hf, pk);
+        }
+        if (C::kSplitP || hf == 1) {
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + 2 * buf + (C::kSplitP ? hf : 0)));
+        }
       }
       uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -596,27 +626,6 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
         // e4m3: the stored P carries the weight 2^lg_pw; l sums unweighted P
         l += C::kFp8 ? tile_sum * ptx::ex2(-lg_pw) : tile_sum;
       }
-      {
-        uint32_t pk[32];
-        if (C::kFp8) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pk[j] = ptx::pack_e4m3x2(s[4 * j], s[4 * j + 1]) |
-                    (ptx::pack_e4m3x2(s[4 * j + 2], s[4 * j + 3]) << 16);
-          ptx::tmem_st32(s_addr, pk);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[2 * j], s[2 * j + 1]);
-          ptx::tmem_st32(s_addr, pk);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[64 + 2 * j], s[64 + 2 * j + 1]);
-          ptx::tmem_st32(s_addr + 32, pk);
-        }
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + buf));
     }
     if (!ok) return;
     // epilogue: O / l (e4m3: O * v_ref * 2^-kappa / l), LSE
@@ -676,7 +685,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     const uint32_t bars = sbase + C::kOffBar;
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
-      if (i == C::kBarPFull || i == C::kBarPFull + 1) count = 4;
+      if (i >= C::kBarPFull && i < C::kBarPFull + 4) count = 4;
       if (i >= C::kBarTileEmpty) count = C::kTileConsumers;
       ptx::mbar_init(bars + 8u * i, count);
     }
