@@ -43,6 +43,7 @@
 #include <cstdint>
 #include <math_constants.h>
 
+#include "exp2_poly.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -70,6 +71,12 @@ struct FwdCfg {
   // lazy-rescale threshold (log2 units) and, for e4m3, the power of two P is
   // scaled by before it is rounded (P * 2^kappa <= 2^(tau + kappa) = 256 < 448)
   static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
+  // share of the exponentials computed by the FMA-pipe polynomial instead of
+  // MUFU (two softmax warps share one sub-partition's MUFU, 8 lanes / cycle):
+  // every kPolyEvery-th pair of scores, 0 = none
+  static constexpr int kPolyEvery = 0;
+  // softmax arithmetic on packed fp32 pairs (fma/add .f32x2) or scalar
+  static constexpr bool kPacked = true;
   // P handed to the MMA warp in two halves of 64 keys (e4m3, where the MMAs
   // are short and the softmax is the critical path) or in one piece (16-bit,
   // where the extra store round trip costs more than it saves)
@@ -94,12 +101,13 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = QT * kTileBytes;
   static constexpr int kOffBar = kOffKV + STAGES * kTileBytes;
-  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2],
+  // barriers: q_full[2], q_empty[2] (per query tile, so the next work tile's
+  // first Q tile loads while this one's last MMAs run), kv_full[S], kv_empty[S], s_full[2],
   // p_full[2][2] (per score buffer, first / second half of the keys),
   // o_full[2], pv_done, mma_done, tile_full[R], tile_empty[R]
   static constexpr int kTileRing = 4;   // work tiles fetched ahead by the load warp
-  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + STAGES,
-                       kBarSFull = 2 + 2 * STAGES, kBarPFull = kBarSFull + 2,
+  static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKVFull = 4, kBarKVEmpty = 4 + STAGES,
+                       kBarSFull = 4 + 2 * STAGES, kBarPFull = kBarSFull + 2,
                        kBarOFull = kBarPFull + 4, kBarPVDone = kBarOFull + 2,
                        kBarMmaDone = kBarPVDone + 1, kBarTileFull = kBarMmaDone + 1,
                        kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
@@ -262,12 +270,14 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     if (w < 0) break;
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
-    if (!wt.wait(bar(C::kBarQEmpty), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
-    ptx::mbar_arrive_expect_tx(bar(C::kBarQFull), C::QT * C::kTileBytes);
 #pragma unroll
-    for (int t = 0; t < C::QT; ++t)
+    for (int t = 0; t < C::QT; ++t) {
+      if (!wt.wait(bar(C::kBarQEmpty + t), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
+      ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
       load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
-                bar(C::kBarQFull));
+                bar(C::kBarQFull + t));
+    }
+    if (!ok) break;
     ++tcount;
     const int n = ti.n_kv;
     const int krow = ti.ktok + 128 * ti.kb0;   // first key row of the tile's range
@@ -290,7 +300,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     const uint32_t first = kvc > (uint32_t)C::STAGES ? kvc - C::STAGES : 0u;
     for (uint32_t c = first; c < kvc; ++c)
       wt.drain(bar(C::kBarKVFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u);
-    if (tcount > 0) wt.drain(bar(C::kBarQFull), (tcount - 1) & 1u);
+    for (int t = 0; t < C::QT && tcount > 0; ++t) wt.drain(bar(C::kBarQFull + t), (tcount - 1) & 1u);
   }
 }
 
@@ -367,7 +377,8 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
   for (int j = 0; ok && next_tile(ring, wt, j, C::kTileRing, false, true, w); ++j) {
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
-    if (!wt.wait(bar(C::kBarQFull), tcount & 1u, 3)) { ok = false; break; }
+    const uint32_t qpar = tcount & 1u;
+    if (!wt.wait(bar(C::kBarQFull), qpar, 3)) { ok = false; break; }
     ++tcount;
     ptx::tc_fence_after();
     const int n = ti.n_kv;
@@ -375,6 +386,9 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
       if (!(ok = kv_ready(kvc))) break;
       qk(C::col_s(0), sq, slot_addr(kvc));
       ptx::mma_commit(bar(C::kBarSFull + 0));
+      if (n == 1) ptx::mma_commit(bar(C::kBarQEmpty + 0));   // last use of Q0
+      if (!(ok = wt.wait(bar(C::kBarQFull + 1), qpar, 3))) break;
+      ptx::tc_fence_after();
       for (int i = 0; i < n; ++i) {
         const uint32_t ck = kvc + 2 * i, cv = ck + 1;
         if (i > 0) {
@@ -384,7 +398,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         qk(C::col_s(1), sq + C::kTileBytes, slot_addr(ck));
         ptx::mma_commit(bar(C::kBarSFull + 1));
         ptx::mma_commit(bar(C::kBarKVEmpty + slot(ck)));
-        if (i == n - 1) ptx::mma_commit(bar(C::kBarQEmpty));
+        if (i == n - 1) ptx::mma_commit(bar(C::kBarQEmpty + 1));   // last use of Q1
         if (!(ok = kv_ready(cv))) break;
         if (!(ok = pv(C::col_o(0), C::col_s(0), slot_addr(cv), i > 0, 0, (it + i) & 1u))) break;
         if (i == n - 1) ptx::mma_commit(bar(C::kBarOFull + 0));
@@ -392,6 +406,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
           if (!(ok = kv_ready(ck + 2))) break;
           qk(C::col_s(0), sq, slot_addr(ck + 2));
           ptx::mma_commit(bar(C::kBarSFull + 0));
+          if (i + 2 == n) ptx::mma_commit(bar(C::kBarQEmpty + 0));   // last use of Q0
         }
       }
       if (!ok) break;
@@ -581,9 +596,20 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
 #pragma unroll
         for (int j = 64 * hf; j < 64 * hf + 64; j += 2) {
           float lo, hi;
-          ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
-          s[j] = ptx::ex2(lo);
-          s[j + 1] = ptx::ex2(hi);
+          if (C::kPacked) {
+            ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
+          } else {
+            lo = fmaf(s[j], c, -mu);
+            hi = fmaf(s[j + 1], c, -mu);
+          }
+          if (C::kPolyEvery > 0 && (j / 2) % C::kPolyEvery == C::kPolyEvery - 1) {
+            ptx::exp2_poly2(lo, hi, kExp2C0, kExp2C1, kExp2C2, kExp2C3);
+            s[j] = lo;
+            s[j + 1] = hi;
+          } else {
+            s[j] = ptx::ex2(lo);
+            s[j + 1] = ptx::ex2(hi);
+          }
         }
         if (masked) {
           // zero the invisible keys after the exponent: with c = 0 their
@@ -612,17 +638,25 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
           if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + 2 * buf + (C::kSplitP ? hf : 0)));
         }
       }
-      uint64_t acc[4] = {0, 0, 0, 0};
+      float tile_sum;
+      if (C::kPacked) {
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int j = 0; j < 128; j += 2)
-        acc[(j >> 1) & 3] = ptx::add2(acc[(j >> 1) & 3], ptx::f2pack(s[j], s[j + 1]));
-      {
+        for (int j = 0; j < 128; j += 2)
+          acc[(j >> 1) & 3] = ptx::add2(acc[(j >> 1) & 3], ptx::f2pack(s[j], s[j + 1]));
         float a0, a1, b0, b1, c0, c1, d0, d1;
         ptx::f2unpack(acc[0], a0, a1);
         ptx::f2unpack(acc[1], b0, b1);
         ptx::f2unpack(acc[2], c0, c1);
         ptx::f2unpack(acc[3], d0, d1);
-        const float tile_sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        tile_sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+      } else {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j & 7] += s[j];
+        tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      }
+      {
         // e4m3: the stored P carries the weight 2^lg_pw; l sums unweighted P
         l += C::kFp8 ? tile_sum * ptx::ex2(-lg_pw) : tile_sum;
       }
