@@ -188,6 +188,25 @@ def oracle_sample(w, inputs, seconds=10.0, max_rows=None):
             "seconds": spent, "rows": rows}
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time (the job finishes when its last rank does).
+    Single process: the value itself. Uses whatever backend the process group
+    was started with (NCCL with a CUDA device on the GPU machine, gloo on CPU)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload, so the
+    job's throughput is all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step a bounded sample."""
     rank = int(os.environ.get("RANK", "0"))
@@ -330,11 +349,7 @@ def main(argv=None):
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), dev)
         per = [sum(m[j].elapsed_time(m[j + 1]) for m in marks) / max(1, len(marks))
                for j in range(len(kernels))] if per_kernel else None
         return ms, per
@@ -343,7 +358,7 @@ def main(argv=None):
         total_ms, per_kernel = timed(step, args.steps, per_kernel=True)
     api.fa_get_device_status(stream)
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_value(flops, world, ms_per_step)
 
     # end to end through the C ABI from pinned host buffers
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
