@@ -51,6 +51,14 @@ def lib():
         L.fa_fp8_prep.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
         L.fa_fwd_fp8.restype = i
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_varlen_blocks.restype = i
+        L.fa_varlen_blocks.argtypes = [vp, i, vp, vp]
+        L.fa_fp8_prep_varlen.restype = i
+        L.fa_fp8_prep_varlen.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp,
+                                         i, i, i, i, i, vp]
+        L.fa_fwd_fp8_varlen.restype = i
+        L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, i, i, i, i, i,
+                                        f, i, vp]
         L.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
         L.fa_fwd_splitkv.restype = i
@@ -178,6 +186,85 @@ def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, Sq, Sk, D, s
     return st
 
 
+def fa_varlen_blocks(cu_seqlens, B, cu_blocks, stream=None, check=True) -> int:
+    """Raw entry point: cu_blocks[b] = sum of ceil(L / 128) over the first b sequences."""
+    st = lib().fa_varlen_blocks(_ptr(cu_seqlens), int(B), _ptr(cu_blocks), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_varlen_blocks")
+    return st
+
+
+def fa_fp8_prep_varlen(q, k, v, q8, k8, v8, q_scale, k_scale, v_scale, sigma, B, H, cu_seqlens_q,
+                       cu_seqlens_k, cu_blocks_q, cu_blocks_k, total_q, total_k, max_seqlen_q, max_seqlen_k, D,
+                       in_dtype=None, stream=None, check=True) -> int:
+    """Raw entry point: ``fa_fp8_prep`` over packed variable-length sequences."""
+    if in_dtype is None:
+        in_dtype = _DTYPE[(q if q is not None else k).dtype]
+    st = lib().fa_fp8_prep_varlen(_ptr(q), _ptr(k), _ptr(v), int(in_dtype), _ptr(q8), _ptr(k8), _ptr(v8),
+                                  _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(sigma), int(B), int(H),
+                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(cu_blocks_q), _ptr(cu_blocks_k),
+                                  int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k), int(D),
+                                  _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fp8_prep_varlen")
+    return st
+
+
+def fa_fwd_fp8_varlen(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, cu_seqlens_q, cu_seqlens_k,
+                      cu_blocks_q, cu_blocks_k, total_q, total_k, max_seqlen_q, max_seqlen_k, D, scale, causal,
+                      stream=None, check=True) -> int:
+    """Raw entry point: ``fa_fwd_fp8`` over packed variable-length sequences."""
+    st = lib().fa_fwd_fp8_varlen(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(o), _ptr(lse), int(B), int(H), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                 _ptr(cu_blocks_q), _ptr(cu_blocks_k), int(total_q), int(total_k),
+                                 int(max_seqlen_q), int(max_seqlen_k), int(D), float(scale), int(bool(causal)),
+                                 _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8_varlen")
+    return st
+
+
+def _fp8_side_varlen(x, cu, H, dev, stream, names):
+    """e4m3 codes, block offsets and scale arrays of one packed side."""
+    B = cu.numel() - 1
+    total = x.shape[0]
+    cb = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    fa_varlen_blocks(cu, B, cb, stream=stream)
+    nb = total // 128 + B   # upper bound on cu_blocks[B]
+    out = {n: torch.empty((nb, H), dtype=torch.float32, device=dev) for n in names[1:]}
+    out[names[0]] = cb
+    return out
+
+
+def fp8_prepare_varlen(q, k, v, sigma, *, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, stream=None):
+    """Varlen ``fp8_prepare``: q ``[total_q, H, D]``, k/v ``[total_k, H, D]``
+    16-bit, ``cu_seqlens_*`` int32 CUDA tensors. Either side may be None (q,
+    or k and v): that side is skipped, so a K/V cache is prepared once and
+    reused. Scale arrays ``[n_blocks, H]`` are allocated at their upper bound
+    ``total // 128 + B`` rows; the first ``cu_blocks[B]`` rows are written."""
+    ref = q if q is not None else k
+    H, D = ref.shape[1], ref.shape[2]
+    dev = ref.device
+    B = (cu_seqlens_q if cu_seqlens_q is not None else cu_seqlens_k).numel() - 1
+    out = {"B": B, "H": H, "D": D, "varlen": True}
+    if q is not None:
+        out.update(_fp8_side_varlen(q, cu_seqlens_q, H, dev, stream, ("cu_blocks_q", "q_scale")))
+        out.update(q8=torch.empty(q.shape, dtype=torch.uint8, device=dev), cu_seqlens_q=cu_seqlens_q,
+                   total_q=q.shape[0], max_seqlen_q=max_seqlen_q)
+    if k is not None:
+        out.update(_fp8_side_varlen(k, cu_seqlens_k, H, dev, stream, ("cu_blocks_k", "k_scale", "v_scale")))
+        out.update(k8=torch.empty(k.shape, dtype=torch.uint8, device=dev),
+                   v8=torch.empty(v.shape, dtype=torch.uint8, device=dev), cu_seqlens_k=cu_seqlens_k,
+                   total_k=k.shape[0], max_seqlen_k=max_seqlen_k)
+    g = out.get
+    fa_fp8_prep_varlen(q, k, v, g("q8"), g("k8"), g("v8"), g("q_scale"), g("k_scale"), g("v_scale"), sigma, B, H,
+                       g("cu_seqlens_q"), g("cu_seqlens_k"), g("cu_blocks_q"), g("cu_blocks_k"), g("total_q", 0),
+                       g("total_k", 0), g("max_seqlen_q", 0) if q is not None else 0,
+                       g("max_seqlen_k", 0) if k is not None else 0, D,
+                       in_dtype=_DTYPE[ref.dtype], stream=stream)
+    return out
+
+
 def fp8_prepare(q, k, v, sigma, *, batch, stream=None):
     """Allocate the e4m3 tensors and block scales and call ``fa_fp8_prep``.
     q ``[B*Sq, H, D]``, k/v ``[B*Sk, H, D]`` 16-bit. Returns a dict."""
@@ -198,7 +285,23 @@ def fp8_prepare(q, k, v, sigma, *, batch, stream=None):
 
 
 def fp8_attention_forward(prep, *, causal=False, scale=None, out=None, lse=None, stream=None):
-    """Attention on the output of ``fp8_prepare``; returns (O bf16, LSE fp32)."""
+    """Attention on the output of ``fp8_prepare`` (or of ``fp8_prepare_varlen``,
+    or a dict merging a Q preparation with a K/V one); returns (O bf16, LSE
+    fp32 ``[B, H, Sq]``, varlen ``[H, total_q]``)."""
+    if prep.get("varlen"):
+        p = prep
+        H, D = p["H"], p["D"]
+        if scale is None:
+            scale = D ** -0.5
+        dev = p["q8"].device
+        if out is None:
+            out = torch.empty((p["total_q"], H, D), dtype=torch.bfloat16, device=dev)
+        if lse is None:
+            lse = torch.empty((H, p["total_q"]), dtype=torch.float32, device=dev)
+        fa_fwd_fp8_varlen(p["q8"], p["k8"], p["v8"], p["q_scale"], p["k_scale"], p["v_scale"], out, lse, p["B"], H,
+                          p["cu_seqlens_q"], p["cu_seqlens_k"], p["cu_blocks_q"], p["cu_blocks_k"], p["total_q"],
+                          p["total_k"], p["max_seqlen_q"], p["max_seqlen_k"], D, scale, causal, stream=stream)
+        return out, lse
     B, H, Sq, Sk, D = prep["B"], prep["H"], prep["Sq"], prep["Sk"], prep["D"]
     if scale is None:
         scale = D ** -0.5

@@ -115,7 +115,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
-int fa_version(void) { return (1 << 16) | 0; }
+int fa_version(void) { return (1 << 16) | 1; }
 
 const char* fa_strerror(int s) {
   switch (s) {
@@ -309,32 +309,39 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   return FA_OK;
 }
 
-int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype, void* q8, void* k8, void* v8,
-                float* q_scale, float* k_scale, float* v_scale, const signed char* sigma, int B, int H,
-                int Sq, int Sk, int D, void* stream) {
+}  // extern "C"
+
+namespace {
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// FP8 preparation, fixed length (cu_* == nullptr; Sq, Sk per sequence) or
+// varlen (cu_seqlens_*, cu_blocks_*, totals; Sq, Sk = max lengths).
+int prep_impl(const void* q, const void* k, const void* v, int in_dtype, void* q8, void* k8, void* v8,
+              float* q_scale, float* k_scale, float* v_scale, const signed char* sigma, int B, int H, int Sq, int Sk,
+              int D, const int* cu_q, const int* cu_k, const int* cbq, const int* cbk, int total_q, int total_k,
+              void* stream) {
   if (in_dtype != FA_FP16 && in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
-  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
-  if ((int64_t)B * Sq > INT32_MAX || (int64_t)B * Sk > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0 || total_q < 0 || total_k < 0) return FA_ERR_INVALID_ARG;
+  const bool varlen = cu_q != nullptr || cu_k != nullptr;
+  if (!varlen && ((int64_t)B * Sq > INT32_MAX || (int64_t)B * Sk > INT32_MAX)) return FA_ERR_INVALID_ARG;
   if (B == 0 || (Sq == 0 && Sk == 0)) return FA_OK;
   const bool has_q = Sq > 0, has_kv = Sk > 0;
   if ((has_q && (!q || !q8 || !q_scale)) || (has_kv && (!k || !v || !k8 || !v8 || !k_scale || !v_scale)))
     return FA_ERR_INVALID_ARG;
-  const void* ptrs16[3] = {q, k, v};
-  for (const void* p : ptrs16)
-    if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return FA_ERR_ALIGNMENT;
-  const void* ptrs8[3] = {q8, k8, v8};
-  for (const void* p : ptrs8)
-    if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return FA_ERR_ALIGNMENT;
-  const void* ptrs32[3] = {q_scale, k_scale, v_scale};
-  for (const void* p : ptrs32)
-    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return FA_ERR_ALIGNMENT;
+  if (varlen && ((has_q && (!cu_q || !cbq)) || (has_kv && (!cu_k || !cbk)))) return FA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, (const void*)q8, (const void*)k8, (const void*)v8})
+    if (p && !aligned16(p)) return FA_ERR_ALIGNMENT;
+  for (const void* p : {(const void*)q_scale, (const void*)k_scale, (const void*)v_scale})
+    if (p && !aligned4(p)) return FA_ERR_ALIGNMENT;
   DevInfo* dev = nullptr;
   int st = current_device(&dev);
   if (st != FA_OK) return st;
-  fa::PrepParams t[3];
+  fa::PrepParams t[3] = {};
   int n = 0;
-  auto add = [&](const void* x, void* x8, float* sc, const signed char* sg, int S) {
+  auto add = [&](const void* x, void* x8, float* sc, const signed char* sg, int S, const int* cu, const int* cb,
+                 int total) {
     fa::PrepParams& P = t[n++];
     P.x = x;
     P.x8 = static_cast<uint8_t*>(x8);
@@ -345,11 +352,15 @@ int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype, void*
     P.S = S;
     P.nblk = (S + 127) / 128;
     P.bf16 = in_dtype == FA_BF16;
+    P.cu_seqlens = cu;
+    P.cu_blocks = cb;
+    P.total = total;
+    P.status = dev->status;
   };
-  if (has_q) add(q, q8, q_scale, sigma, Sq);
+  if (has_q) add(q, q8, q_scale, sigma, Sq, cu_q, cbq, total_q);
   if (has_kv) {
-    add(k, k8, k_scale, sigma, Sk);
-    add(v, v8, v_scale, nullptr, Sk);
+    add(k, k8, k_scale, sigma, Sk, cu_k, cbk, total_k);
+    add(v, v8, v_scale, nullptr, Sk, cu_k, cbk, total_k);
   }
   cudaError_t e = fa::launch_fp8_prep(t, n, D, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -359,21 +370,23 @@ int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype, void*
   return FA_OK;
 }
 
-int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
-               const float* v_scale, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
-               int causal, void* stream) {
+int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
+                 int causal, const int* cu_q, const int* cu_k, const int* cbq, const int* cbk, int total_q,
+                 int total_k, void* stream) {
   if (D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  const int64_t Tq = (int64_t)B * Sq, Tk = (int64_t)B * Sk;
+  const bool varlen = cu_q != nullptr || cu_k != nullptr;
+  if (varlen && (!cu_q || !cu_k || !cbq || !cbk || total_q < 0 || total_k < 0)) return FA_ERR_INVALID_ARG;
+  const int64_t Tq = varlen ? total_q : (int64_t)B * Sq, Tk = varlen ? total_k : (int64_t)B * Sk;
   if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
-  if (B == 0 || Sq == 0) return FA_OK;
+  if (B == 0 || Sq == 0 || Tq == 0) return FA_OK;
   if (!q8 || !k8 || !v8 || !o || !lse || !q_scale || (Sk > 0 && (!k_scale || !v_scale)))
     return FA_ERR_INVALID_ARG;
-  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
-      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned4(lse) ||
+      !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))
     return FA_ERR_ALIGNMENT;
   const int rows = fa::cta_rows(D);
   const int64_t n_qblk = ((int64_t)Sq + rows - 1) / rows;
@@ -392,6 +405,10 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_sc
   if ((st = make_map(&L.tv, v8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
   L.p.o = o;
   L.p.lse = lse;
+  L.p.cu_q = cu_q;
+  L.p.cu_k = cu_k;
+  L.p.cu_blocks_q = cbq;
+  L.p.cu_blocks_k = cbk;
   L.p.B = B;
   L.p.H = H;
   L.p.Sq = Sq;
@@ -421,6 +438,56 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_sc
     return FA_ERR_CUDA;
   }
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype, void* q8, void* k8, void* v8,
+                float* q_scale, float* k_scale, float* v_scale, const signed char* sigma, int B, int H,
+                int Sq, int Sk, int D, void* stream) {
+  return prep_impl(q, k, v, in_dtype, q8, k8, v8, q_scale, k_scale, v_scale, sigma, B, H, Sq, Sk, D, nullptr,
+                   nullptr, nullptr, nullptr, 0, 0, stream);
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
+               int causal, void* stream) {
+  return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, Sq, Sk, D, scale, causal, nullptr,
+                      nullptr, nullptr, nullptr, 0, 0, stream);
+}
+
+int fa_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, void* stream) {
+  if (B < 0 || (B > 0 && (!cu_seqlens || !cu_blocks))) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+  if (fa::launch_varlen_blocks(cu_seqlens, B, cu_blocks, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fp8_prep_varlen(const void* q, const void* k, const void* v, int in_dtype, void* q8, void* k8, void* v8,
+                       float* q_scale, float* k_scale, float* v_scale, const signed char* sigma, int B, int H,
+                       const int* cu_seqlens_q, const int* cu_seqlens_k, const int* cu_blocks_q,
+                       const int* cu_blocks_k, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                       int D, void* stream) {
+  if ((max_seqlen_q > 0 && !cu_seqlens_q) || (max_seqlen_k > 0 && !cu_seqlens_k)) return FA_ERR_INVALID_ARG;
+  return prep_impl(q, k, v, in_dtype, q8, k8, v8, q_scale, k_scale, v_scale, sigma, B, H, max_seqlen_q,
+                   max_seqlen_k, D, cu_seqlens_q, cu_seqlens_k, cu_blocks_q, cu_blocks_k, total_q, total_k, stream);
+}
+
+int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                      const float* v_scale, void* o, float* lse, int B, int H, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, const int* cu_blocks_q, const int* cu_blocks_k, int total_q,
+                      int total_k, int max_seqlen_q, int max_seqlen_k, int D, float scale, int causal,
+                      void* stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k || !cu_blocks_q || !cu_blocks_k) return FA_ERR_INVALID_ARG;
+  return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, max_seqlen_q, max_seqlen_k, D, scale,
+                      causal, cu_seqlens_q, cu_seqlens_k, cu_blocks_q, cu_blocks_k, total_q, total_k, stream);
 }
 
 int fa_get_device_status(void* stream, int* raw) {

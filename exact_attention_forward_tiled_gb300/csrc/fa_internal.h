@@ -44,6 +44,10 @@ struct FwdParams {
   int n_split, split_blocks;
   float* o_part;
   float* lse_part;
+  // e4m3 varlen: prefix sums of the per-sequence 128-row block counts; the
+  // scales are then [cu_blocks[B], H] (nullptr: fixed length, [B, H, nblk])
+  const int* cu_blocks_q;
+  const int* cu_blocks_k;
 };
 
 // Element kinds of the attention inputs.
@@ -73,13 +77,18 @@ cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
 
 // FP8 preparation: rotation (optional) + block quantisation of one tensor.
 struct PrepParams {
-  const void* x;        // [B*S, H, D] 16-bit input
-  uint8_t* x8;          // [B*S, H, D] e4m3 output
-  float* scale;         // [B, H, nblk] fp32 output
+  const void* x;        // [tokens, H, D] 16-bit input
+  uint8_t* x8;          // [tokens, H, D] e4m3 output
+  float* scale;         // fixed: [B, H, nblk]; varlen: [cu_blocks[B], H] fp32 output
   const int8_t* sigma;  // [D] +-1, or nullptr: no rotation
-  int B, H, S, nblk;
+  int B, H, S, nblk;    // varlen: S = max length, nblk = ceil(S / 128)
   int bf16;             // 1: bf16 input, 0: fp16
+  const int* cu_seqlens;  // varlen: [B + 1] token prefix sums, or nullptr
+  const int* cu_blocks;   // varlen: [B + 1] prefix sums of ceil(L_b / 128)
+  int total;              // varlen: rows of x
+  int* status;            // device status word (bad cu_seqlens entries)
 };
+cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, cudaStream_t stream);
 cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cudaStream_t stream);
 
 }  // namespace fa

@@ -61,6 +61,26 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) f
   const int rest = bid / P.H;
   const int b = rest % P.B;
   const int blk = rest / P.B;
+  // the block's rows: tokens start + [blk * 128, min(blk * 128 + 128, L))
+  int64_t start = (int64_t)b * P.S;
+  int L = P.S;
+  int64_t sidx = ((int64_t)b * P.H + h) * P.nblk + blk;   // where its scale goes
+  if (P.cu_seqlens != nullptr) {
+    const int s0 = __ldg(P.cu_seqlens + b), s1 = __ldg(P.cu_seqlens + b + 1);
+    const int c0 = __ldg(P.cu_blocks + b), c1 = __ldg(P.cu_blocks + b + 1), cn = __ldg(P.cu_blocks + P.B);
+    // bad lengths, or block offsets that do not span exactly this sequence's
+    // blocks within the first cu_blocks[B] <= total / 128 + B rows of the
+    // [n_blocks, H] scale arrays: skipped and reported
+    if (s0 < 0 || s1 < s0 || s1 > P.total || s1 - s0 > P.S || c0 < 0 || c1 - c0 != (s1 - s0 + 127) / 128 ||
+        c1 > cn || cn > P.total / 128 + P.B) {
+      if (threadIdx.x == 0 && blk == 0 && h == 0) atomicOr(P.status, kDevBadSeqlens);
+      return;
+    }
+    start = s0;
+    L = s1 - s0;
+    if (blk * 128 >= L) return;   // the whole CTA leaves together
+    sidx = (int64_t)(c0 + blk) * P.H + h;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPR;              // row of the instruction this lane serves
   const int d0 = (lane % LPR) * 8;         // first element of the lane
@@ -76,8 +96,8 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) f
 #pragma unroll
   for (int i = 0; i < ITER; ++i) {
     const int row = blk * 128 + warp * RPW + i * RPI + sub;
-    if (row < P.S) {
-      load8(P, (((int64_t)b * P.S + row) * P.H + h) * D + d0, x[i]);
+    if (row < L) {
+      load8(P, ((start + row) * P.H + h) * D + d0, x[i]);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
@@ -126,18 +146,36 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) f
   amax *= norm;   // amax of the rotated, normalised values
   const float scale = amax > 0.f ? amax / 448.f : 1.f;
   const float inv = norm / scale;
-  if (threadIdx.x == 0) P.scale[((int64_t)b * P.H + h) * P.nblk + blk] = scale;
+  if (threadIdx.x == 0) P.scale[sidx] = scale;
 
 #pragma unroll
   for (int i = 0; i < ITER; ++i) {
     const int row = blk * 128 + warp * RPW + i * RPI + sub;
-    if (row >= P.S) continue;
+    if (row >= L) continue;
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
-    *reinterpret_cast<uint2*>(P.x8 + (((int64_t)b * P.S + row) * P.H + h) * D + d0) =
+    *reinterpret_cast<uint2*>(P.x8 + ((start + row) * P.H + h) * D + d0) =
         make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
   }
+}
+
+// cu_blocks[b] = sum over b' < b of ceil(L_b' / 128), L_b = cu_seqlens[b+1] - cu_seqlens[b]
+// (a negative length counts as 0). One thread: B is small next to the rest.
+__global__ void varlen_blocks_kernel(const int* __restrict__ cu_seqlens, int B, int* __restrict__ cu_blocks) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int acc = 0;
+  cu_blocks[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = cu_seqlens[b + 1] - cu_seqlens[b];
+    acc += L > 0 ? (L + 127) / 128 : 0;
+    cu_blocks[b + 1] = acc;
+  }
+}
+
+cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, cudaStream_t stream) {
+  varlen_blocks_kernel<<<1, 32, 0, stream>>>(cu_seqlens, B, cu_blocks);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cudaStream_t stream) {

@@ -157,8 +157,19 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
     t.Lq = qe - qs;
     t.Lk = ke - ks;
     // a sequence that breaks the declared bounds is skipped (and reported)
-    if (qs < 0 || qe < qs || qe > p.total_q || ks < 0 || ke < ks || ke > p.total_k ||
-        t.Lq > p.Sq || t.Lk > p.Sk) {
+    bool bad = qs < 0 || qe < qs || qe > p.total_q || ks < 0 || ke < ks || ke > p.total_k ||
+               t.Lq > p.Sq || t.Lk > p.Sk;
+    if (!bad && p.cu_blocks_q != nullptr) {
+      // e4m3 block-scale offsets: this sequence's entries must span exactly its
+      // blocks and stay inside the first total / 128 + B rows of the
+      // [n_blocks, H] scale arrays
+      const int bq0 = __ldg(p.cu_blocks_q + t.b), bq1 = __ldg(p.cu_blocks_q + t.b + 1);
+      const int bk0 = __ldg(p.cu_blocks_k + t.b), bk1 = __ldg(p.cu_blocks_k + t.b + 1);
+      const int bqn = __ldg(p.cu_blocks_q + p.B), bkn = __ldg(p.cu_blocks_k + p.B);
+      bad = bq0 < 0 || bq1 - bq0 != (t.Lq + 127) / 128 || bq1 > bqn || bqn > p.total_q / 128 + p.B ||
+            bk0 < 0 || bk1 - bk0 != (t.Lk + 127) / 128 || bk1 > bkn || bkn > p.total_k / 128 + p.B;
+    }
+    if (bad) {
       t.Lq = 0;
       t.Lk = 0;
       if (qblk == 0) atomicOr(p.status, kDevBadSeqlens);
@@ -502,13 +513,26 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     float c_q = p.c, v_ref = 1.f;
     const float* ks_row = nullptr;
     const float* vs_row = nullptr;
+    int sstride = 1;   // between the scales of consecutive blocks
     if (C::kFp8) {
-      const int64_t hb = (int64_t)ti.b * p.H + ti.h;
-      c_q = p.c * __ldg(p.q_scale + hb * p.nblk_q + min(ti.qblk * C::QT + t, p.nblk_q - 1));
-      ks_row = p.k_scale + hb * p.nblk_k;
-      vs_row = p.v_scale + hb * p.nblk_k;
+      // block scales: [B, H, nblk] (fixed length) or [n_blocks, H] (varlen,
+      // block g = cu_blocks[b] + blk counted per sequence, heads fastest)
+      const int nq = (ti.Lq + 127) / 128, nk = (ti.Lk + 127) / 128;
+      const float* qs_row;
+      if (p.cu_blocks_q != nullptr) {
+        sstride = p.H;
+        qs_row = p.q_scale + (int64_t)__ldg(p.cu_blocks_q + ti.b) * p.H + ti.h;
+        ks_row = p.k_scale + (int64_t)__ldg(p.cu_blocks_k + ti.b) * p.H + ti.h;
+        vs_row = p.v_scale + (int64_t)__ldg(p.cu_blocks_k + ti.b) * p.H + ti.h;
+      } else {
+        const int64_t hb = (int64_t)ti.b * p.H + ti.h;
+        qs_row = p.q_scale + hb * p.nblk_q;
+        ks_row = p.k_scale + hb * p.nblk_k;
+        vs_row = p.v_scale + hb * p.nblk_k;
+      }
+      c_q = p.c * __ldg(qs_row + (int64_t)min(ti.qblk * C::QT + t, nq - 1) * sstride);
       float vmax = 0.f;
-      for (int j = 0; j < p.nblk_k; ++j) vmax = fmaxf(vmax, __ldg(vs_row + j));
+      for (int j = 0; j < nk; ++j) vmax = fmaxf(vmax, __ldg(vs_row + (int64_t)j * sstride));
       v_ref = vmax > 0.f ? vmax : 1.f;
     }
     const float inv_vref = 1.f / v_ref;
@@ -517,9 +541,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     bool ok = true;
     for (int i = 0; i < ti.n_kv; ++i, ++it) {
       const int kb = ti.kb0 + i;   // absolute 128-key block
-      const float c = C::kFp8 ? c_q * __ldg(ks_row + kb) : c_q;
+      const float c = C::kFp8 ? c_q * __ldg(ks_row + (int64_t)kb * sstride) : c_q;
       // log2 of the factor the stored P carries: 2^kappa * v_s(j) / v_ref (e4m3 only)
-      const float lg_pw = C::kFp8 ? ptx::lg2(__ldg(vs_row + kb) * inv_vref) + C::kLog2Kappa : 0.f;
+      const float lg_pw =
+          C::kFp8 ? ptx::lg2(__ldg(vs_row + (int64_t)kb * sstride) * inv_vref) + C::kLog2Kappa : 0.f;
       const int buf = C::QT == 2 ? t : (int)(it & 1u);
       const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
       if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;

@@ -164,12 +164,77 @@ int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype,
  *   q8, k8, v8 and the three scale arrays as written by fa_fp8_prep
  *   o            bf16 [B*Sq, H, D] (written); lse fp32 [B, H, Sq] (written)
  *   D            128 or 256 (64 -> FA_ERR_UNSUPPORTED)
- *   scale, causal as for fa_fwd. Fixed length only.
+ *   scale, causal as for fa_fwd. Fixed length (varlen: fa_fwd_fp8_varlen).
  */
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
                const float* q_scale, const float* k_scale, const float* v_scale,
                void* o, float* lse, int B, int H, int Sq, int Sk, int D,
                float scale, int causal, void* stream);
+
+/*
+ * fa_varlen_blocks -- block offsets of the variable-length e4m3 layout.
+ *
+ *   cu_seqlens   device int32 [B + 1], token prefix sums (as for fa_fwd)
+ *   cu_blocks    device int32 [B + 1] (written): cu_blocks[0] = 0,
+ *                cu_blocks[b + 1] = cu_blocks[b] + ceil(L_b / 128),
+ *                L_b = cu_seqlens[b + 1] - cu_seqlens[b] (a negative L_b
+ *                counts as 0 and is reported later by the kernels that use it)
+ *
+ * One small kernel on `stream`; nothing is read on the host. The varlen
+ * scales of a tensor are fp32 [n_blocks, H]: row cu_blocks[b] + j holds the
+ * scales of block j of sequence b for every head. cu_blocks[B] never exceeds
+ * floor(total / 128) + B, the number of rows to allocate when the host does
+ * not know the lengths.
+ */
+int fa_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, void* stream);
+
+/*
+ * fa_fp8_prep_varlen -- fa_fp8_prep over packed variable-length sequences
+ * ("FlashAttention-3 (lukebest wiki)", technique 3, applied per sequence).
+ *
+ *   q, k, v      16-bit [total_q, H, D] and [total_k, H, D]
+ *   q8, k8, v8   e4m3 outputs of the same shapes (written)
+ *   cu_seqlens_q/k  device int32 [B + 1] token prefix sums
+ *   cu_blocks_q/k   device int32 [B + 1] from fa_varlen_blocks on them
+ *   q_scale      fp32 [cu_blocks_q[B], H] (written); k_scale, v_scale
+ *                fp32 [cu_blocks_k[B], H] (written)
+ *   max_seqlen_q/k  bounds on the lengths; 0 skips that side (Q, or K and
+ *                V), whose pointers may then be NULL -- K and V of a cache
+ *                are prepared once and reused with every new Q
+ *
+ * Blocks are the 128-row blocks of each sequence, counted from its first
+ * token; a sequence's last block may be short. A sequence whose entries break
+ * the bounds (negative or decreasing offsets, beyond total, longer than
+ * max_seqlen, or cu_blocks not matching the lengths) is skipped and reported
+ * as FA_ERR_DEVICE_SEQLENS by fa_get_device_status.
+ */
+int fa_fp8_prep_varlen(const void* q, const void* k, const void* v, int in_dtype,
+                       void* q8, void* k8, void* v8, float* q_scale, float* k_scale, float* v_scale,
+                       const signed char* sigma, int B, int H,
+                       const int* cu_seqlens_q, const int* cu_seqlens_k,
+                       const int* cu_blocks_q, const int* cu_blocks_k,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D, void* stream);
+
+/*
+ * fa_fwd_fp8_varlen -- fa_fwd_fp8 over packed variable-length sequences, on
+ * the output of fa_fp8_prep_varlen.
+ *
+ *   o            bf16 [total_q, H, D] (written); lse fp32 [H, total_q]
+ *                (written)
+ *   cu_*, total_*, max_seqlen_* as for fa_fp8_prep_varlen (all required)
+ *   D            128 or 256; scale, causal as for fa_fwd (the causal
+ *                diagonal is bottom-right aligned per sequence)
+ *
+ * Bad sequences are skipped (their rows left unwritten) and reported as
+ * FA_ERR_DEVICE_SEQLENS by fa_get_device_status.
+ */
+int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
+                      const float* q_scale, const float* k_scale, const float* v_scale,
+                      void* o, float* lse, int B, int H,
+                      const int* cu_seqlens_q, const int* cu_seqlens_k,
+                      const int* cu_blocks_q, const int* cu_blocks_k,
+                      int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D,
+                      float scale, int causal, void* stream);
 
 /*
  * fa_get_device_status -- synchronise `stream`, then read and clear the

@@ -63,3 +63,34 @@ def test_valid_call_without_gpu_reports_no_device(L):
     assert _call(L) == -7
     raw = ctypes.c_int(0)
     assert L.fa_get_device_status(None, ctypes.byref(raw)) == -7
+
+
+def _fp8_varlen(L, cq=0x6000, ck=0x7000, cbq=0x8000, cbk=0x9000, tq=300, tk=300, mq=128, mk=128, D=128,
+                o=0x4000, scale=0.1):
+    return L.fa_fwd_fp8_varlen(0x1000, 0x2000, 0x3000, 0xa000, 0xb000, 0xc000, o, 0x5000, 2, 2, cq, ck, cbq,
+                               cbk, tq, tk, mq, mk, D, ctypes.c_float(scale), 0, None)
+
+
+def _prep_varlen(L, q=0x1000, k=0x2000, cq=0x6000, ck=0x7000, cbq=0x8000, cbk=0x9000, mq=128, mk=128, D=128,
+                 dtype=api.FA_BF16, qs=0xa000):
+    return L.fa_fp8_prep_varlen(q, k, 0x3000, dtype, 0x11000, 0x12000, 0x13000, qs, 0xb000, 0xc000, None, 2, 2,
+                                cq, ck, cbq, cbk, 300, 300, mq, mk, D, None)
+
+
+def test_fp8_varlen_host_argument_checks(L):
+    # every cu_seqlens / cu_blocks array is required by the forward
+    for kw in ("cq", "ck", "cbq", "cbk"):
+        assert _fp8_varlen(L, **{kw: None}) == -1, kw
+    assert _fp8_varlen(L, D=64) == -2
+    assert _fp8_varlen(L, tq=-1) == -1 and _fp8_varlen(L, scale=-2.0) == -1
+    assert _fp8_varlen(L, o=0x4008) == -3
+    assert _fp8_varlen(L, mq=0) == 0                   # no query rows: a no-op
+    # the preparation needs the arrays of each side it prepares, and only those
+    assert _prep_varlen(L, cq=None) == -1 and _prep_varlen(L, cbk=None) == -1
+    assert _prep_varlen(L, dtype=api.FA_FP8_E4M3) == -2 and _prep_varlen(L, D=96) == -2
+    assert _prep_varlen(L, q=0x1004) == -3 and _prep_varlen(L, qs=0xa002) == -3
+    assert _prep_varlen(L, mq=0, mk=0) == 0
+    assert L.fa_varlen_blocks(None, 3, 0x8000, None) == -1 and L.fa_varlen_blocks(0x6000, -1, 0x8000, None) == -1
+    import torch
+    if not torch.cuda.is_available():
+        assert _fp8_varlen(L) == -7 and _prep_varlen(L) == -7 and _prep_varlen(L, q=None, cq=None, mq=0) == -7
