@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for exact tiled attention forward.
+"""fp64 CPU oracle for exact tiled attention: the forward and its gradients.
 
 TEST INFRASTRUCTURE ONLY. The only code that may import, call, link or run
 anything in this package is the test suite (``tests/``), the smoke check in
@@ -27,6 +27,12 @@ Parity status of each function (what pins it; see tests/test_oracle_*.py):
   H H^T = D I, M M^T = I, (QM)(KM)^T = QK^T.
 * ``e4m3_encode`` / ``e4m3_decode`` -- pinned: exhaustive against torch's
   ``float8_e4m3fn`` casts.
+* ``attention_backward_head`` / ``attention_backward`` -- pinned: central
+  finite differences of the C forward (an independent route to the same
+  derivative), closed forms (single key, scale = 0), invariants (dK rows sum
+  to zero, dV rows sum to the dO rows, linearity in dO).
+* ``attention_backward_sampled`` -- pinned: equals ``attention_backward_head``
+  at every row on small inputs.
 * ``block_scales`` / ``fp8_attention_emulated`` -- parity unpinned beyond the
   special cases in the tests: the block granularity, the amax/448 scale and
   the rule that quantises P are readings of pages that leave them open.
@@ -232,6 +238,105 @@ def visible_pairs(qpos, Lk, Lq, causal) -> int:
     """Number of (row, visible key) pairs of the given rows."""
     qpos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
     return int(_load().oracle_visible_pairs(qpos.ctypes.data, len(qpos), int(Lk), int(Lq), int(bool(causal))))
+
+
+# --------------------------------------------------------------------------
+# gradients of exact attention (the backward pass)
+# --------------------------------------------------------------------------
+def _visible(Lq, Lk, causal, qpos=None):
+    """Boolean [n, Lk] mask of the keys each row sees (bottom-right aligned
+    causal mask: row i sees keys j <= i + Lk - Lq)."""
+    qpos = np.arange(Lq) if qpos is None else np.asarray(qpos, dtype=np.int64)
+    j = np.arange(Lk)[None, :]
+    if not causal:
+        return np.ones((len(qpos), Lk), dtype=bool)
+    return j <= qpos[:, None] + (Lk - Lq)
+
+
+def attention_backward_head(q, k, v, do, scale, causal):
+    """Gradients of one (sequence, head) pair: (dQ, dK, dV) in fp64.
+
+    The pages print no backward formula ("FlashAttention-3 (lukebest wiki)"
+    only reports its speed); this is the exact derivative of the forward of
+    "Flash Attention 3 principles (guijiagi)" section 1.2 (S = scale QK^T
+    with the section 5.2 causal mask, P = softmax(S) row by row, O = PV) for
+    an upstream gradient dO, written out from the chain rule:
+
+        dV = P^T dO
+        dP = dO V^T
+        dS_ij = P_ij (dP_ij - sum_l P_il dP_il)     (softmax Jacobian, row i)
+        dQ = scale dS K,   dK = scale dS^T Q
+
+    Masked pairs have P = 0 and so dS = 0; a row with no visible key has
+    O = 0 and contributes nothing. Plain numpy on whole matrices.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    Lq, Lk = q.shape[0], k.shape[0]
+    vis = _visible(Lq, Lk, causal)
+    s = np.where(vis, scale * (q @ k.T), -np.inf)
+    m = s.max(axis=1, initial=-np.inf, where=vis) if Lk else np.full(Lq, -np.inf)
+    m = np.where(np.isfinite(m), m, 0.0)
+    e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    tot = e.sum(axis=1)
+    p = np.divide(e, tot[:, None], out=np.zeros_like(e), where=tot[:, None] > 0)
+    dv = p.T @ do
+    dp = do @ v.T
+    ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv
+
+
+def attention_backward(q, k, v, do, *, scale, causal, nseq, Sq=None, Sk=None,
+                       cu_seqlens_q=None, cu_seqlens_k=None):
+    """``attention_backward_head`` over a packed ``[tokens, H, D]`` batch
+    (fixed length or ``cu_seqlens`` packing, as ``attention``). Returns
+    (dQ, dK, dV) fp64 with the shapes of q, k, v."""
+    H = q.shape[1]
+    bq, bk = _seq_bounds(nseq, Sq, Sk, cu_seqlens_q, cu_seqlens_k)
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(nseq):
+        qs, qe = bq[b]
+        ks, ke = bk[b]
+        for h in range(H):
+            g = attention_backward_head(q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], do[qs:qe, h], scale, causal)
+            dq[qs:qe, h], dk[ks:ke, h], dv[ks:ke, h] = g
+    return dq, dk, dv
+
+
+def attention_backward_sampled(q, k, v, do, q_rows, k_rows, *, scale, causal):
+    """Gradients of one (sequence, head) pair at some rows only, for problems
+    too large for ``attention_backward_head``: dQ at query rows ``q_rows``,
+    dK and dV at key rows ``k_rows``.
+
+    Same definition, evaluated a row or a column of P at a time: the row
+    normalisers LSE_i and O_i come from the C forward (``attention_head``),
+    P_ij = exp(scale q_i.k_j - LSE_i) on visible pairs, and the Jacobian term
+    sum_l P_il dP_il is taken as dO_i . O_i, which equals it exactly
+    (sum_l P_il dO_i.v_l = dO_i . sum_l P_il v_l). Returns (dQ [nq, D],
+    dK [nk, D], dV [nk, D]).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    Lq, Lk = q.shape[0], k.shape[0]
+    o, lse = attention_head(q, np.arange(Lq), k, v, Lq, scale, causal)
+    delta = (do * o).sum(axis=1)
+    lse_safe = np.where(np.isfinite(lse), lse, np.inf)     # rows with no key: P = 0
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    # rows of P for dQ
+    vis = _visible(Lq, Lk, causal, q_rows)
+    pr = np.where(vis, np.exp(scale * (q[q_rows] @ k.T) - lse_safe[q_rows, None]), 0.0)
+    dsr = pr * ((do[q_rows] @ v.T) - delta[q_rows, None])
+    dq = scale * (dsr @ k)
+    # columns of P for dK, dV
+    visc = _visible(Lq, Lk, causal)[:, k_rows]
+    pc = np.where(visc, np.exp(scale * (q @ k[k_rows].T) - lse_safe[:, None]), 0.0)
+    dsc = pc * ((do @ v[k_rows].T) - delta[:, None])
+    dk = scale * (dsc.T @ q)
+    dv = pc.T @ do
+    return dq, dk, dv
 
 
 # --------------------------------------------------------------------------
