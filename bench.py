@@ -15,6 +15,12 @@ the outputs copied back inside the timed region. ``roofline`` compares the
 kernel with the measured dense bf16 tensor-core peak; ``cpu_baseline`` times
 the fp64 oracle on the host cores on a bounded sample of the same workload.
 
+Backward workloads (``--workload b1`` / ``b2``): a step is one ``fa_bwd``
+call (row constants, dK/dV kernel, dQ kernel) for O, LSE from one forward run
+before timing; the metric counts 2.5x the forward's FLOPs (the five matrix
+products of the gradient) and ``e2e`` copies Q, K, V, O, dO, LSE in and dQ,
+dK, dV out every step.
+
 ``--impl reference`` times the oracle itself as the reference arm (each step
 a bounded sample of the workload) and prints the same line with
 "impl": "reference".
@@ -38,6 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of measured dense tensor-core ceiling"
+METRIC_BWD = "attention bwd TFLOP/s (2.5x forward FLOPs) on 1 GB300 and % of measured dense tensor-core ceiling"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -188,6 +195,42 @@ def oracle_sample(w, inputs, seconds=10.0, max_rows=None):
             "seconds": spent, "rows": rows}
 
 
+def oracle_bwd_sample(w, inputs, seconds=10.0, rows=None):
+    """Time the oracle's gradients on a bounded sample of a backward workload:
+    the leading ``rows`` x ``rows`` square (queries and keys) of (sequence,
+    head) pairs in order, whole-matrix fp64 numpy, until ``seconds`` pass. The
+    square is sized from a small probe so one pair takes about a second."""
+    from oracle import oracle as orc
+    import numpy as np
+    scale = w.D ** -0.5
+    if rows is None:
+        n0 = min(512, w.Sq)
+        t0 = time.perf_counter()
+        orc.attention_backward_head(*(orc._f64(inputs[t][:n0, 0, :]) for t in ("q", "k", "v", "do")), scale,
+                                    w.causal)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        rows = int(min(w.Sq, max(256, n0 * (1.0 / dt) ** 0.5)))
+    spent, flops, pairs = 0.0, 0.0, 0
+    for b in range(w.B):
+        for h in range(w.H):
+            s0 = b * w.Sq
+            args = [orc._f64(inputs[t][s0:s0 + rows, h, :]) for t in ("q", "k", "v", "do")]
+            t0 = time.perf_counter()
+            orc.attention_backward_head(*args, scale, w.causal)
+            spent += time.perf_counter() - t0
+            flops += 10.0 * rows * rows * w.D * (0.5 if w.causal else 1.0)
+            pairs += 1
+            if spent >= seconds:
+                break
+        if spent >= seconds:
+            break
+    return {"value": flops / spent / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{pairs} (sequence, head) pairs of {w.name} cut to their first {rows} queries and keys, "
+                      f"fp64 numpy gradients (BLAS on all host cores), {spent:.2f} s; FLOPs counted as "
+                      f"2.5x the forward's",
+            "seconds": spent, "rows": rows}
+
+
 def max_over_ranks(ms: float, device=None) -> float:
     """The slowest rank's time (the job finishes when its last rank does).
     Single process: the value itself. Uses whatever backend the process group
@@ -218,17 +261,26 @@ def run_reference(args):
     orc.build()
     w = workloads.WORKLOADS[args.workload]
     inputs = workloads.make_inputs(w, device="cpu")
-    # one step = the rows of the first (sequence, head) that take ~1 s
-    probe = oracle_sample(w, inputs, seconds=0.0, max_rows=256)
-    rows = max(16, int(256 * 1.0 / max(probe["seconds"], 1e-3)))
     vals = []
-    for i in range(args.warmup + args.steps):
-        r = oracle_sample(w, inputs, seconds=1e9, max_rows=rows)
-        if i >= args.warmup:
-            vals.append(r)
+    if w.backward:
+        # one step = the gradients of the first (sequence, head) cut to a
+        # square that takes ~1 s
+        probe = oracle_bwd_sample(w, inputs, seconds=0.0)
+        for i in range(args.warmup + args.steps):
+            r = oracle_bwd_sample(w, inputs, seconds=0.0, rows=probe["rows"])
+            if i >= args.warmup:
+                vals.append(r)
+    else:
+        # one step = the rows of the first (sequence, head) that take ~1 s
+        probe = oracle_sample(w, inputs, seconds=0.0, max_rows=256)
+        rows = max(16, int(256 * 1.0 / max(probe["seconds"], 1e-3)))
+        for i in range(args.warmup + args.steps):
+            r = oracle_sample(w, inputs, seconds=1e9, max_rows=rows)
+            if i >= args.warmup:
+                vals.append(r)
     tot_s = sum(r["seconds"] for r in vals)
     value = statistics.mean(r["value"] for r in vals)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / len(vals),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
@@ -300,32 +352,49 @@ def main(argv=None):
         flops = A.attention_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
         extra = {}
 
-    # one step = the whole hot path; for fp8 the prep kernel then the attention.
-    # hot_path(q, k, v, o, lse, stream) returns the list of its launches.
-    if fp8:
+    # one step = the whole hot path; for fp8 the prep kernel then the attention;
+    # for a backward workload one fa_bwd call (row constants, dK/dV, dQ).
+    # hot_path(ins, outs, stream) returns the list of its launches; `ins` are
+    # the step's inputs (copied from the host in the end-to-end loop), `outs`
+    # its results (copied back).
+    ins, outs = [q, k, v], [o, lse]
+    if w.backward:
+        do = inputs["do"]
+        api.attention_forward(q, k, v, causal=w.causal, scale=scale, batch=w.B, out=o, lse=lse)
+        ins = [q, k, v, o, do, lse]   # the order of fa_bwd's arguments
+        outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+        ws_bytes = api.fa_bwd_workspace_size(w.H, q.shape[0])
+        bwd_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        flops = A.attention_bwd_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
+
+        def hot_path(i_, o_, st):
+            return [lambda: api.fa_bwd(*i_, *o_, w.B, w.H, Sq, Sk, w.D, scale, w.causal, workspace=bwd_ws,
+                                       workspace_bytes=ws_bytes, stream=st)]
+        names = ["fa_bwd (bwd_prep_kernel + fa_bwd_kernel dK/dV + fa_bwd_kernel dQ)"]
+    elif fp8:
         prep = api.fp8_prepare(q, k, v, inputs["sigma"], batch=w.B, stream=stream)
 
-        def hot_path(qq, kk, vv, oo, ll, st):
+        def hot_path(i_, o_, st):
+            qq, kk, vv = i_
             return [lambda: api.fa_fp8_prep(qq, kk, vv, prep["q8"], prep["k8"], prep["v8"], prep["q_scale"],
                                             prep["k_scale"], prep["v_scale"], inputs["sigma"], w.B, w.H, Sq, Sk,
                                             w.D, stream=st),
-                    lambda: api.fp8_attention_forward(prep, causal=w.causal, scale=scale, out=oo, lse=ll,
+                    lambda: api.fp8_attention_forward(prep, causal=w.causal, scale=scale, out=o_[0], lse=o_[1],
                                                       stream=st)]
         names = ["fp8_prep_kernel", "fa_fwd_kernel"]
     elif w.splitkv:
         ws_bytes = api.fa_fwd_splitkv_workspace_size(w.B, w.H, Sq, Sk, w.D, 0)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
-        def hot_path(qq, kk, vv, oo, ll, st):
-            return [lambda: api.fa_fwd_splitkv(qq, kk, vv, oo, ll, w.B, w.H, Sq, Sk, w.D, scale, w.causal, 0,
+        def hot_path(i_, o_, st):
+            return [lambda: api.fa_fwd_splitkv(*i_, *o_, w.B, w.H, Sq, Sk, w.D, scale, w.causal, 0,
                                                workspace, ws_bytes, stream=st)]
         names = ["fa_fwd_kernel+splitkv_merge_kernel"]
     else:
-        def hot_path(qq, kk, vv, oo, ll, st):
-            return [lambda: api.fa_fwd(qq, kk, vv, oo, ll, w.B, w.H, Sq, Sk, w.D, scale, w.causal, stream=st,
-                                       **extra)]
+        def hot_path(i_, o_, st):
+            return [lambda: api.fa_fwd(*i_, *o_, w.B, w.H, Sq, Sk, w.D, scale, w.causal, stream=st, **extra)]
         names = ["fa_fwd_kernel"]
-    kernels = list(zip(names, hot_path(q, k, v, o, lse, stream)))
+    kernels = list(zip(names, hot_path(ins, outs, stream)))
 
     def step():
         for _, fn in kernels:
@@ -370,15 +439,14 @@ def main(argv=None):
     value = job_value(flops, world, ms_per_step)
 
     # end to end through the C ABI from pinned host buffers: every step copies
-    # its inputs in and its outputs (O and LSE) out. Copies and compute of
-    # neighbouring steps overlap (H2D and D2H on their own streams, two sets of
-    # device buffers), as a serving loop would run them.
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    # its inputs in and its results out. Copies and compute of neighbouring
+    # steps overlap (H2D and D2H on their own streams, two sets of device
+    # buffers), as a serving loop would run them.
+    in_host = [t.cpu().pin_memory() for t in ins]
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d_st, d2h_st = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    sets = [(q, k, v, o, lse)] + [tuple(torch.empty_like(t) for t in (q, k, v, o, lse))]
-    runs = [hot_path(*bset, stream) for bset in sets]
+    sets = [(ins, outs), ([torch.empty_like(t) for t in ins], [torch.empty_like(t) for t in outs])]
+    runs = [hot_path(i_, o_, stream) for i_, o_ in sets]
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_ready = [ev(), ev()]
     out_ready = [ev(), ev()]
@@ -390,12 +458,11 @@ def main(argv=None):
     def e2e_loop(steps):
         for i in range(steps):
             b = i % 2
-            qd, kd, vd, od, ld = sets[b]
+            i_dev, o_dev = sets[b]
             h2d_st.wait_event(in_free[b])
             with torch.cuda.stream(h2d_st):
-                qd.copy_(qh, non_blocking=True)
-                kd.copy_(kh, non_blocking=True)
-                vd.copy_(vh, non_blocking=True)
+                for d_, h_ in zip(i_dev, in_host):
+                    d_.copy_(h_, non_blocking=True)
             in_ready[b].record(h2d_st)
             stream.wait_event(in_ready[b])
             stream.wait_event(out_free[b])
@@ -405,8 +472,8 @@ def main(argv=None):
             out_ready[b].record(stream)
             d2h_st.wait_event(out_ready[b])
             with torch.cuda.stream(d2h_st):
-                oh.copy_(od, non_blocking=True)
-                lh.copy_(ld, non_blocking=True)
+                for h_, d_ in zip(out_host, o_dev):
+                    h_.copy_(d_, non_blocking=True)
             out_free[b].record(d2h_st)
 
     e2e_loop(3)
@@ -423,8 +490,8 @@ def main(argv=None):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), dev) / e2e_steps
     api.fa_get_device_status(stream)
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in in_host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
 
     peaks, peak_src = load_peaks()
     attn_ms = per_kernel[-1]
@@ -437,10 +504,14 @@ def main(argv=None):
         peak = peaks["bf16_tflops"]
         peak_note = f"{peak_src} bf16 dense GEMM (burst), MEASURED_PEAKS.json"
     kern = "fa_fwd_kernel"
+    if w.backward:
+        kern = "fa_bwd"
+        peak_note += ("; achieved = algorithmic backward FLOPs (5 matrix products, 2.5x the forward's) over "
+                      "the whole fa_bwd call (3 kernels; the dQ kernel recomputes S and dP, 7 products run)")
     if w.splitkv:
         peak_note += "; achieved covers the attention and the merge kernel of each call"
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if fp8 else w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": Sq, "Sk": Sk, "D": w.D,
@@ -448,7 +519,9 @@ def main(argv=None):
                    "l2": "inputs larger than L2 (no flush between steps)",
                    "inputs": "Q,K,V iid N(0,1) fp32 -> %s, seed %d%s" % (
                        "bf16" if fp8 else w.dtype, w.seed,
-                       ", 0.1%% N(0,10^2) outliers in 4 columns, prep + attention per step" if fp8 else "")},
+                       ", 0.1%% N(0,10^2) outliers in 4 columns, prep + attention per step" if fp8 else
+                       (", dO iid N(0,1); O, LSE from one forward before timing; one fa_bwd per step"
+                        if w.backward else ""))},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": committed_traffic(kern, w.name),
                      "peak_source": peak_note, "kernel": kern, "kernel_ms": attn_ms},
@@ -456,10 +529,11 @@ def main(argv=None):
                            "frac": achieved / (ceiling * (2.0 if fp8 else 1.0))},
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "note": "pinned host -> device copy of Q, K, V and device -> host copy of O, LSE every "
-                        "step; copies of neighbouring steps overlap compute (two buffer sets, "
-                        "H2D / D2H streams)"},
-        "gpu_launches": args.steps * (2 if w.splitkv else len(kernels)),
+                "note": ("pinned host -> device copy of Q, K, V, O, LSE, dO and device -> host copy of dQ, "
+                         "dK, dV every step" if w.backward else
+                         "pinned host -> device copy of Q, K, V and device -> host copy of O, LSE every step")
+                        + "; copies of neighbouring steps overlap compute (two buffer sets, H2D / D2H streams)"},
+        "gpu_launches": args.steps * (3 if w.backward else 2 if w.splitkv else len(kernels)),
         "clocks": clk.summary(),
     }
     if fp8:
@@ -470,8 +544,12 @@ def main(argv=None):
                                  "kernel_ms": per_kernel[0], "bytes": pb,
                                  "traffic": committed_traffic("fp8_prep_kernel", w.name)}
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        cb = oracle_sample(w, {"q": q.cpu(), "k": k.cpu(), "v": v.cpu(),
-                               "cu_seqlens_q": inputs["cu_seqlens_q"]}, seconds=args.cpu_seconds)
+        host = {"q": q.cpu(), "k": k.cpu(), "v": v.cpu(), "cu_seqlens_q": inputs["cu_seqlens_q"]}
+        if w.backward:
+            host["do"] = inputs["do"].cpu()
+            cb = oracle_bwd_sample(w, host, seconds=args.cpu_seconds)
+        else:
+            cb = oracle_sample(w, host, seconds=args.cpu_seconds)
         cb.pop("seconds")
         cb.pop("rows")
         line["cpu_baseline"] = cb

@@ -22,6 +22,13 @@ def attention_flops(H, D, lengths_q, lengths_k, causal) -> float:
     return total
 
 
+def attention_bwd_flops(H, D, lengths_q, lengths_k, causal) -> float:
+    """Backward FLOPs by the usual convention: five matrix products of
+    2 * Sq * Sk * D each (S, dP, dV, dK, dQ), i.e. 2.5x the forward's, halved
+    under the causal mask. Recomputation beyond them is not counted."""
+    return 2.5 * attention_flops(H, D, lengths_q, lengths_k, causal)
+
+
 def attention_exps(H, lengths_q, lengths_k, causal) -> float:
     total = 0.0
     for lq, lk in zip(lengths_q, lengths_k):

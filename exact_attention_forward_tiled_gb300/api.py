@@ -59,6 +59,11 @@ def lib():
         L.fa_fwd_fp8_varlen.restype = i
         L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, i, i, i, i, i,
                                         f, i, vp]
+        L.fa_bwd_workspace_size.restype = ctypes.c_size_t
+        L.fa_bwd_workspace_size.argtypes = [i, i]
+        L.fa_bwd.restype = i
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, i, i, vp,
+                             ctypes.c_size_t, i, vp]
         L.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
         L.fa_fwd_splitkv.restype = i
@@ -357,3 +362,45 @@ def attention_forward(q, k, v, *, causal=False, scale=None, cu_seqlens_q=None, c
     fa_fwd(q, k, v, out, lse, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q, cu_seqlens_k,
            q.shape[0], k.shape[0], stream=stream)
     return out, lse
+
+
+def fa_bwd_workspace_size(H, total_q) -> int:
+    return int(lib().fa_bwd_workspace_size(int(H), int(total_q)))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q=None,
+           cu_seqlens_k=None, total_q=0, total_k=0, workspace=None, workspace_bytes=0, dtype=None, stream=None,
+           check=True) -> int:
+    """Raw entry point: dQ, dK, dV of the attention forward for upstream gradient dO."""
+    if dtype is None:
+        dtype = _DTYPE[q.dtype]
+    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                      int(B), int(H), int(Sq), int(Sk), int(D), float(scale), int(bool(causal)),
+                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(total_q), int(total_k), _ptr(workspace),
+                      int(workspace_bytes), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return st
+
+
+def attention_backward(q, k, v, o, lse, dout, *, causal=False, scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
+                       max_seqlen_q=None, max_seqlen_k=None, batch=None, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the scratch) and call ``fa_bwd``. Arguments
+    as ``attention_forward``; ``o`` and ``lse`` are its outputs, ``dout`` the
+    gradient of ``o``. Returns (dQ, dK, dV)."""
+    H, D = q.shape[1], q.shape[2]
+    if cu_seqlens_q is None:
+        B = batch
+        Sq, Sk = q.shape[0] // B, k.shape[0] // B
+    else:
+        B = cu_seqlens_q.numel() - 1
+        Sq, Sk = max_seqlen_q, max_seqlen_k
+    if scale is None:
+        scale = D ** -0.5
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa_bwd_workspace_size(H, q.shape[0])
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, scale, causal, cu_seqlens_q, cu_seqlens_k,
+           q.shape[0], k.shape[0], workspace, workspace.numel() * workspace.element_size(), stream=stream)
+    return dq, dk, dv

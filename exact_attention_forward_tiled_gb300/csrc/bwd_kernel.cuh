@@ -1,0 +1,536 @@
+// Exact attention backward for sm_103a (GB300): dQ, dK, dV of
+// O = softmax(scale * Q K^T [+ causal mask]) V for an upstream gradient dO.
+//
+// The pages give the forward only ("Flash Attention 3 principles (guijiagi)"
+// section 1.2 with the section 2.2 softmax; the "FlashAttention-3 (lukebest
+// wiki)" table reports backward speed without the algorithm). The gradient
+// is the plain derivative of that forward:
+//
+//   P = exp(scale * S - LSE)     (recomputed tile by tile from the forward's LSE)
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - Delta),   Delta = rowsum(dO * O)
+//   dQ = scale * dS K,   dK = scale * dS^T Q
+//
+// Two persistent kernels share this template (deterministic, no atomics):
+//
+//   dK/dV kernel: a CTA keeps one 128-key block of K and V in shared memory
+//     and streams the 128-row blocks of Q and dO that can see it:
+//       S^T = K Q^T, dP^T = V dO^T          (tcgen05, both operands in SMEM)
+//       P^T, dS^T -> 16-bit, back into tensor memory over S^T, dP^T
+//       dV += P^T dO, dK += dS^T Q          (tcgen05, A from tensor memory)
+//   dQ kernel: a CTA keeps one 128-row block of Q and dO and streams K, V:
+//       S = Q K^T, dP = dO V^T;  P, dS -> tensor memory;  dQ += dS K
+//
+// The dQ kernel recomputes S and dP (7 instead of 5 matrix products in all)
+// so that every output row is written by exactly one CTA.
+//
+// Roles: eight "softmax" warps (two warpgroups, each owning half of the 128
+// streamed columns of every resident row: thread = resident row), one MMA
+// warp (one thread issues), one load warp (TMA). Every mbarrier wait is
+// bounded (see pipeline.cuh).
+#pragma once
+
+#include <cstdint>
+#include <math_constants.h>
+
+#include "fa_internal.h"
+#include "pipeline.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D_, int STAGES_, int KIND_, bool DQ_>
+struct BwdCfg {
+  static constexpr int D = D_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int KIND = KIND_;
+  static constexpr bool DQ = DQ_;
+  static constexpr int kBoxCols = 64;               // 16-bit elements per 128-byte box row
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kBoxBytes = 128 * 128;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;   // one 128-row tile
+  static constexpr int kKSteps = D / 16;                 // MMA K steps over D
+  static constexpr int kSoftmaxWarps = 8;
+  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  static constexpr int kThreads = 320;
+  static constexpr int kTmemCols = 512;
+  // tensor memory: accumulators at 0 (dQ, or dV) and D (dK); X (S or S^T)
+  // at 256 and Y (dP or dP^T) at 384; the 16-bit P / dS go over X / Y
+  static constexpr uint32_t kColAcc1 = DQ ? 0u : (uint32_t)D;   // dQ or dK
+  static constexpr uint32_t kColAcc2 = 0u;                      // dV
+  static constexpr uint32_t kColX = 256u, kColY = 384u;
+  // shared memory
+  static constexpr int kOffR = 0;                                // R1, R2
+  static constexpr int kOffT = 2 * kTileBytes;                   // ring of T tiles
+  static constexpr int kOffVec = kOffT + STAGES * kTileBytes;    // per-warp column constants
+  static constexpr int kVecBytes = 2 * 64 * 4;                   // -lse2[64], -delta[64]
+  static constexpr int kOffBar = kOffVec + kSoftmaxWarps * kVecBytes;
+  static constexpr int kTileRing = 4;
+  static constexpr int kBarRFull = 0, kBarREmpty = 1, kBarTFull = 2, kBarTEmpty = 2 + STAGES,
+                       kBarSFull = 2 + 2 * STAGES, kBarZFull = kBarSFull + 1, kBarAccFull = kBarZFull + 1,
+                       kBarMmaDone = kBarAccFull + 1, kBarTileFull = kBarMmaDone + 1,
+                       kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
+  static constexpr int kTileConsumers = 1 + kSoftmaxWarps;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
+
+  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(2 * D <= 256, "accumulators below the score columns");
+};
+
+// Work tile: one 128-row block of the resident side of one (sequence, head).
+struct BwdTile {
+  int b, h;
+  int r0;          // first resident row within its sequence
+  int Lq, Lk;
+  int rtok, ttok;  // token of row 0 of the sequence on the resident / streamed side
+  int t_first;     // first streamed 128-row block
+  int n_t;         // streamed blocks to visit
+  bool live;       // false: the block starts beyond its sequence
+};
+
+template <bool DQ, bool CAUSAL>
+__device__ __forceinline__ BwdTile bwd_tile(const BwdParams& p, int w) {
+  BwdTile t;
+  const int bh = w / p.n_rblk;
+  const int j = w - bh * p.n_rblk;
+  // causal: heavy tiles first (dQ: the last query blocks see the most keys;
+  // dK/dV: the first key blocks are seen by the most queries)
+  const int rblk = (DQ && CAUSAL) ? p.n_rblk - 1 - j : j;
+  t.b = bh / p.H;
+  t.h = bh - t.b * p.H;
+  int qs, ks;
+  if (p.cu_q != nullptr) {
+    qs = __ldg(p.cu_q + t.b);
+    const int qe = __ldg(p.cu_q + t.b + 1);
+    ks = __ldg(p.cu_k + t.b);
+    const int ke = __ldg(p.cu_k + t.b + 1);
+    t.Lq = qe - qs;
+    t.Lk = ke - ks;
+    if (qs < 0 || qe < qs || qe > p.total_q || ks < 0 || ke < ks || ke > p.total_k || t.Lq > p.Sq ||
+        t.Lk > p.Sk) {
+      t.Lq = 0;
+      t.Lk = 0;
+      if (rblk == 0) atomicOr(p.status, kDevBadSeqlens);
+    }
+  } else {
+    qs = t.b * p.Sq;
+    ks = t.b * p.Sk;
+    t.Lq = p.Sq;
+    t.Lk = p.Sk;
+  }
+  t.r0 = rblk * 128;
+  const int shift = t.Lk - t.Lq;   // causal: query i sees keys j <= i + shift
+  t.t_first = 0;
+  t.n_t = 0;
+  if (DQ) {
+    t.rtok = qs;
+    t.ttok = ks;
+    t.live = t.r0 < t.Lq;
+    if (t.live) {
+      const int last = min(t.r0 + 128, t.Lq) - 1;
+      const int lim = CAUSAL ? min(t.Lk, last + shift + 1) : t.Lk;
+      t.n_t = lim > 0 ? (lim + 127) / 128 : 0;
+    }
+  } else {
+    t.rtok = ks;
+    t.ttok = qs;
+    t.live = t.r0 < t.Lk;
+    if (t.live) {
+      const int q_lo = CAUSAL ? max(0, t.r0 - shift) : 0;   // first query that sees key r0
+      if (q_lo < t.Lq) {
+        t.t_first = q_lo / 128;
+        t.n_t = (t.Lq + 127) / 128 - t.t_first;
+      }
+    }
+  }
+  return t;
+}
+
+__device__ __forceinline__ int bwd_fetch_tile(const BwdParams& p, int j) {
+  const int w = j == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(p.sched, 1u);
+  return w < p.ntiles ? w : -1;
+}
+
+// ------------------------------------------------------------------ load warp (lane 0)
+template <class C, bool CAUSAL>
+__device__ void bwd_load_role(const CUtensorMap* tr1, const CUtensorMap* tr2, const CUtensorMap* tt1,
+                              const CUtensorMap* tt2, const BwdParams& p, uint32_t sbase, const Waiter& wt,
+                              const TileRing& ring) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t tc = 0, rcount = 0;
+  bool ok = true;
+  auto load_tile = [&](const CUtensorMap* m, int h, int row, uint32_t dst, uint32_t b) {
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxes; ++bx)
+      ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
+  };
+  auto load_t = [&](const CUtensorMap* m, int h, int row) -> bool {
+    const int s = tc % C::STAGES;
+    const uint32_t ph = (tc / C::STAGES) & 1u;
+    if (!wt.wait(bar(C::kBarTEmpty + s), ph ^ 1u, 22)) return false;
+    ptx::mbar_arrive_expect_tx(bar(C::kBarTFull + s), C::kTileBytes);
+    load_tile(m, h, row, sbase + C::kOffT + s * C::kTileBytes, bar(C::kBarTFull + s));
+    ++tc;
+    return true;
+  };
+
+  for (int j = 0; ok; ++j) {
+    const int rs = j % C::kTileRing;
+    if (!wt.wait(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 29)) break;
+    const int w = bwd_fetch_tile(p, j);
+    ring.slots[rs] = w;
+    ptx::mbar_arrive(ring.full(rs));
+    if (w < 0) break;
+    const BwdTile ti = bwd_tile<C::DQ, CAUSAL>(p, w);
+    if (!ti.live || ti.n_t == 0) continue;
+    if (!wt.wait(bar(C::kBarREmpty), (rcount & 1u) ^ 1u, 21)) break;
+    ptx::mbar_arrive_expect_tx(bar(C::kBarRFull), 2 * C::kTileBytes);
+    load_tile(tr1, ti.h, ti.rtok + ti.r0, sbase + C::kOffR, bar(C::kBarRFull));
+    load_tile(tr2, ti.h, ti.rtok + ti.r0, sbase + C::kOffR + C::kTileBytes, bar(C::kBarRFull));
+    ++rcount;
+    for (int i = 0; ok && i < ti.n_t; ++i) {
+      const int row = ti.ttok + 128 * (ti.t_first + i);
+      ok = load_t(tt1, ti.h, row) && load_t(tt2, ti.h, row);
+    }
+  }
+  if (*wt.abort_flag) {
+    const uint32_t first = tc > (uint32_t)C::STAGES ? tc - C::STAGES : 0u;
+    for (uint32_t c = first; c < tc; ++c)
+      wt.drain(bar(C::kBarTFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u);
+    if (rcount > 0) wt.drain(bar(C::kBarRFull), (rcount - 1) & 1u);
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp (one thread)
+template <class C, bool CAUSAL>
+__device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
+                             const TileRing& ring) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  constexpr uint32_t fmt = C::KIND == kBF16 ? 1u : 0u;
+  constexpr uint32_t idesc_s = ptx::make_idesc(fmt, false, 128, 128);   // X, Y: 128 x 128
+  constexpr uint32_t idesc_acc = ptx::make_idesc(fmt, true, 128, C::D); // acc += Z T (T MN-major)
+  const uint32_t r1 = sbase + C::kOffR, r2 = r1 + C::kTileBytes;
+  auto slot_addr = [&](uint32_t c) { return sbase + C::kOffT + (c % C::STAGES) * C::kTileBytes; };
+
+  // X or Y = R T^T over the head dimension (both K-major)
+  auto mm_s = [&](uint32_t col, uint32_t r_addr, uint32_t t_addr) {
+#pragma unroll
+    for (int kk = 0; kk < C::kKSteps; ++kk) {
+      const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+      ptx::mma_f16_ss(tmem + col, ptx::smem_desc_sw128(r_addr + off, 16, 1024),
+                      ptx::smem_desc_sw128(t_addr + off, 16, 1024), idesc_s, kk > 0);
+    }
+  };
+  // acc (+)= Z T: Z (16-bit, in tensor memory over X or Y; warpgroup g's 64
+  // streamed rows packed at columns 64 g .. 64 g + 31) times the T tile
+  // (MN-major B: 16 streamed rows per step)
+  auto mm_acc = [&](uint32_t acc_col, uint32_t z_col, uint32_t t_addr, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t zc = z_col + 64u * (kk >> 2) + 8u * (kk & 3);
+      const uint64_t b = ptx::smem_desc_sw128(t_addr + kk * 16 * 128, C::kBoxBytes, 1024);
+      ptx::mma_f16_ts(tmem + acc_col, tmem + zc, b, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+  auto t_ready = [&](uint32_t c) {
+    const bool r = wt.wait(bar(C::kBarTFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u, 23);
+    ptx::tc_fence_after();
+    return r;
+  };
+
+  uint32_t tc = 0, it = 0, rcount = 0;
+  bool ok = true;
+  int w = 0;
+  for (int j = 0; ok && next_tile(ring, wt, j, C::kTileRing, false, true, w); ++j) {
+    const BwdTile ti = bwd_tile<C::DQ, CAUSAL>(p, w);
+    if (!ti.live || ti.n_t == 0) continue;
+    if (!(ok = wt.wait(bar(C::kBarRFull), rcount & 1u, 24))) break;
+    ++rcount;
+    ptx::tc_fence_after();
+    for (int i = 0; i < ti.n_t; ++i, ++it) {
+      const uint32_t c1 = tc, c2 = tc + 1;
+      tc += 2;
+      if (!(ok = t_ready(c1))) break;
+      mm_s(C::kColX, r1, slot_addr(c1));
+      if (!(ok = t_ready(c2))) break;
+      mm_s(C::kColY, r2, slot_addr(c2));
+      ptx::mma_commit(bar(C::kBarSFull));
+      if (i == ti.n_t - 1) ptx::mma_commit(bar(C::kBarREmpty));   // last use of R1, R2
+      if (!(ok = wt.wait(bar(C::kBarZFull), it & 1u, 25))) break;
+      ptx::tc_fence_after();
+      // dQ kernel: dQ += dS K.  dK/dV kernel: dK += dS^T Q, dV += P^T dO
+      mm_acc(C::kColAcc1, C::kColY, slot_addr(c1), i > 0);
+      if (!C::DQ) mm_acc(C::kColAcc2, C::kColX, slot_addr(c2), i > 0);
+      ptx::mma_commit(bar(C::kBarTEmpty + (int)(c1 % C::STAGES)));
+      ptx::mma_commit(bar(C::kBarTEmpty + (int)(c2 % C::STAGES)));
+    }
+    if (!ok) break;
+    ptx::mma_commit(bar(C::kBarAccFull));
+  }
+  ptx::mma_commit(bar(C::kBarMmaDone));
+  wt.drain(bar(C::kBarMmaDone), 0);
+}
+
+// ------------------------------------------------------------------ softmax warps
+template <int KIND>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  return KIND == kF16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
+}
+
+// Write one output row (D values, times `mul`) from tensor-memory columns
+// [col, col + n) into out[0 .. n) as 16-bit.
+template <int KIND>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, int n, float mul, uint16_t* out, bool write) {
+#pragma unroll 1
+  for (int ch = 0; ch < n / 32; ++ch) {
+    uint32_t v[32];
+    ptx::tmem_ld32(taddr + 32 * ch, v);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      pk[j] = pack16<KIND>(__uint_as_float(v[2 * j]) * mul, __uint_as_float(v[2 * j + 1]) * mul);
+    if (write) {
+      uint4* dst = reinterpret_cast<uint4*>(out + 32 * ch);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void zero_row(uint16_t* out, int n, bool write) {
+  if (!write) return;
+  for (int d = 0; d < n; d += 8) *reinterpret_cast<uint4*>(out + d) = make_uint4(0, 0, 0, 0);
+}
+
+template <class C, bool CAUSAL>
+__device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                                 const Waiter& wt, const TileRing& ring, int warp) {
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  const int lane = threadIdx.x & 31;
+  const int quarter = warp & 3, g = warp >> 2;
+  const int r = quarter * 32 + lane;                            // resident row within the block
+  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
+  float* vec = reinterpret_cast<float*>(smem + C::kOffVec + warp * C::kVecBytes);   // -lse2[64], -delta[64]
+  const float c = p.c;
+  const uint64_t c2 = ptx::f2pack(c, c);
+
+  uint32_t it = 0, acount = 0;
+  int w = 0;
+  for (int jt = 0; next_tile(ring, wt, jt, C::kTileRing, true, lane == 0, w); ++jt) {
+    const BwdTile ti = bwd_tile<C::DQ, CAUSAL>(p, w);
+    if (!ti.live) continue;
+    const int row = ti.r0 + r;                         // resident row within the sequence
+    const bool row_ok = row < (C::DQ ? ti.Lq : ti.Lk);
+    const int64_t tok = (int64_t)ti.rtok + row;
+    uint16_t* out1 = reinterpret_cast<uint16_t*>(p.dr1) + (tok * p.H + ti.h) * C::D;
+    uint16_t* out2 = C::DQ ? nullptr : reinterpret_cast<uint16_t*>(p.dr2) + (tok * p.H + ti.h) * C::D;
+    if (ti.n_t == 0) {
+      // no pair of this block is visible: zero gradient rows
+      if (C::DQ) {
+        zero_row<C::KIND>(out1 + g * (C::D / 2), C::D / 2, row_ok);
+      } else {
+        zero_row<C::KIND>(g == 0 ? out1 : out2, C::D, row_ok);
+      }
+      continue;
+    }
+    const int shift = ti.Lk - ti.Lq;
+    // dQ kernel: this row's constants; visible keys [0, k_hi)
+    float nl_row = 0.f, nd_row = 0.f;
+    int k_hi = 0;
+    // dK/dV kernel: this key's visible queries [q_lo, Lq)
+    int q_lo = 0;
+    if (C::DQ) {
+      if (row_ok) {
+        const int64_t qi = (int64_t)ti.h * p.total_q + tok;
+        nl_row = -__ldg(p.lse2 + qi);
+        nd_row = -__ldg(p.delta + qi);
+      }
+      k_hi = row_ok ? (CAUSAL ? min(ti.Lk, row + shift + 1) : ti.Lk) : 0;
+    } else {
+      q_lo = CAUSAL ? row - shift : 0;
+    }
+    bool ok = true;
+    for (int i = 0; i < ti.n_t; ++i, ++it) {
+      const int tb = ti.t_first + i;             // streamed block within the sequence
+      const int col0 = 128 * tb + 64 * g;        // first streamed row of this warpgroup's half
+      if (!C::DQ) {
+        // this warpgroup's 64 query columns: -lse2 and -delta (0 beyond the sequence)
+        const float* l2 = p.lse2 + (int64_t)ti.h * p.total_q + ti.ttok;
+        const float* dl = p.delta + (int64_t)ti.h * p.total_q + ti.ttok;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int qq = col0 + lane + 32 * k;
+          const bool in = qq < ti.Lq;
+          vec[lane + 32 * k] = in ? -__ldg(l2 + qq) : 0.f;
+          vec[64 + lane + 32 * k] = in ? -__ldg(dl + qq) : 0.f;
+        }
+        __syncwarp();
+      }
+      if (!(ok = wt.wait_warp(bar(C::kBarSFull), it & 1u, 26))) break;
+      ptx::tc_fence_after();
+      // visible columns of this thread: [lo, hi) relative to col0
+      int lo, hi;
+      if (C::DQ) {
+        lo = 0;
+        hi = k_hi - col0;
+      } else {
+        lo = q_lo - col0;
+        hi = row_ok ? ti.Lq - col0 : 0;
+      }
+      // two chunks of 32 columns; chunk ch's 16-bit results go to columns
+      // 64 g + 16 ch, which this warpgroup has already read
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t xv[32], yv[32];
+        ptx::tmem_ld32(tl + C::kColX + 64 * g + 32 * ch, xv);
+        ptx::tmem_ld32(tl + C::kColY + 64 * g + 32 * ch, yv);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(xv);
+        ptx::reg_fence(yv);
+        const int clo = lo - 32 * ch, chi = hi - 32 * ch;
+        const bool masked = clo > 0 || chi < 32;
+        uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          uint64_t nl2, nd2;
+          if (C::DQ) {
+            nl2 = ptx::f2pack(nl_row, nl_row);
+            nd2 = ptx::f2pack(nd_row, nd_row);
+          } else {
+            const float2 a = *reinterpret_cast<const float2*>(vec + 32 * ch + j);
+            const float2 b = *reinterpret_cast<const float2*>(vec + 64 + 32 * ch + j);
+            nl2 = ptx::f2pack(a.x, a.y);
+            nd2 = ptx::f2pack(b.x, b.y);
+          }
+          float e0, e1;
+          ptx::f2unpack(ptx::fma2(ptx::f2pack(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1])), c2, nl2),
+                        e0, e1);
+          float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+          if (masked) {
+            p0 = (j >= clo && j < chi) ? p0 : 0.f;
+            p1 = (j + 1 >= clo && j + 1 < chi) ? p1 : 0.f;
+          }
+          const uint64_t t = ptx::add2(ptx::f2pack(__uint_as_float(yv[j]), __uint_as_float(yv[j + 1])), nd2);
+          float d0, d1;
+          ptx::f2unpack(ptx::mul2(ptx::f2pack(p0, p1), t), d0, d1);
+          pk_p[j >> 1] = pack16<C::KIND>(p0, p1);
+          pk_ds[j >> 1] = pack16<C::KIND>(d0, d1);
+        }
+        if (!C::DQ) ptx::tmem_st16(tl + C::kColX + 64 * g + 16 * ch, pk_p);
+        ptx::tmem_st16(tl + C::kColY + 64 * g + 16 * ch, pk_ds);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarZFull));
+    }
+    if (!ok) return;
+    if (!wt.wait_warp(bar(C::kBarAccFull), acount & 1u, 27)) return;
+    ++acount;
+    ptx::tc_fence_after();
+    if (C::DQ) {
+      store_acc_row<C::KIND>(tl + C::kColAcc1 + g * (C::D / 2), C::D / 2, p.scale, out1 + g * (C::D / 2), row_ok);
+    } else if (g == 0) {
+      store_acc_row<C::KIND>(tl + C::kColAcc1, C::D, p.scale, out1, row_ok);   // dK
+    } else {
+      store_acc_row<C::KIND>(tl + C::kColAcc2, C::D, 1.f, out2, row_ok);       // dV
+    }
+    // the next tile's first accumulating MMA overwrites these columns only
+    // after this warp's next Z hand-off
+    ptx::tc_fence_before();
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, int STAGES, int KIND, bool DQ, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tr1, const __grid_constant__ CUtensorMap tr2,
+                  const __grid_constant__ CUtensorMap tt1, const __grid_constant__ CUtensorMap tt2,
+                  const BwdParams p) {
+  using C = BwdCfg<D, STAGES, KIND, DQ>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  if (threadIdx.x == 0) {
+    const uint32_t bars = sbase + C::kOffBar;
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i == C::kBarZFull) count = C::kSoftmaxWarps;
+      if (i >= C::kBarTileEmpty) count = C::kTileConsumers;
+      ptx::mbar_init(bars + 8u * i, count);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    ptx::prefetch_tmap(&tr1);
+    ptx::prefetch_tmap(&tr2);
+    ptx::prefetch_tmap(&tt1);
+    ptx::prefetch_tmap(&tt2);
+  }
+  if (warp == C::kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const Waiter wt{abort_flag, p.status};
+  const TileRing ring{sbase + C::kOffBar + 8u * C::kBarTileFull, sbase + C::kOffBar + 8u * C::kBarTileEmpty,
+                      reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16)};
+  if (warp == C::kLoadWarp) {
+    if (lane == 0) bwd_load_role<C, CAUSAL>(&tr1, &tr2, &tt1, &tt2, p, sbase, wt, ring);
+  } else if (warp == C::kMmaWarp) {
+    if (lane == 0) bwd_mma_role<C, CAUSAL>(p, sbase, tmem, wt, ring);
+  } else {
+    bwd_softmax_role<C, CAUSAL>(p, sbase, smem, tmem, wt, ring, warp);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
+}
+
+template <int D, int STAGES, int KIND, bool DQ>
+cudaError_t launch_bwd_dir(const BwdLaunch& L) {
+  using C = BwdCfg<D, STAGES, KIND, DQ>;
+  auto kern = L.causal ? fa_bwd_kernel<D, STAGES, KIND, DQ, true> : fa_bwd_kernel<D, STAGES, KIND, DQ, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = L.p.ntiles < L.num_sms ? L.p.ntiles : L.num_sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tr1, L.tr2, L.tt1, L.tt2, L.p);
+  return cudaGetLastError();
+}
+
+template <int D, int STAGES>
+cudaError_t launch_bwd_impl(const BwdLaunch& L) {
+  if (L.kind == kF16)
+    return L.dq ? launch_bwd_dir<D, STAGES, kF16, true>(L) : launch_bwd_dir<D, STAGES, kF16, false>(L);
+  return L.dq ? launch_bwd_dir<D, STAGES, kBF16, true>(L) : launch_bwd_dir<D, STAGES, kBF16, false>(L);
+}
+
+}  // namespace fa

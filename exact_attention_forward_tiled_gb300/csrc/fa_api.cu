@@ -115,7 +115,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
-int fa_version(void) { return (1 << 16) | 1; }
+int fa_version(void) { return (1 << 16) | 2; }
 
 const char* fa_strerror(int s) {
   switch (s) {
@@ -488,6 +488,102 @@ int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8, const floa
   if (!cu_seqlens_q || !cu_seqlens_k || !cu_blocks_q || !cu_blocks_k) return FA_ERR_INVALID_ARG;
   return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, max_seqlen_q, max_seqlen_k, D, scale,
                       causal, cu_seqlens_q, cu_seqlens_k, cu_blocks_q, cu_blocks_k, total_q, total_k, stream);
+}
+
+size_t fa_bwd_workspace_size(int H, int total_q) {
+  if (H <= 0 || total_q <= 0) return 0;
+  return round256((size_t)2 * (size_t)H * (size_t)total_q * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, float scale, int causal,
+           const int* cu_seqlens_q, const int* cu_seqlens_k, int total_q, int total_k, void* workspace,
+           size_t workspace_bytes, int dtype, void* stream) {
+  // ---- host-side argument checks (no device access)
+  if (dtype == FA_FP8_E4M3) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
+  if (varlen && (total_q < 0 || total_k < 0)) return FA_ERR_INVALID_ARG;
+  const int64_t Tq = varlen ? total_q : (int64_t)B * Sq;
+  const int64_t Tk = varlen ? total_k : (int64_t)B * Sk;
+  if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)H * D * 2 > (int64_t)1 << 38) return FA_ERR_INVALID_ARG;
+  if (B == 0 || (Tq == 0 && Tk == 0)) return FA_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+    if (!aligned16(p)) return FA_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGNMENT;
+  const size_t need = fa_bwd_workspace_size(H, (int)Tq);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_ALIGNMENT;
+  const int64_t nq = ((int64_t)Sq + 127) / 128, nk = ((int64_t)Sk + 127) / 128;
+  if ((int64_t)B * H * nq > INT32_MAX || (int64_t)B * H * nk > INT32_MAX) return FA_ERR_INVALID_ARG;
+
+  // ---- device
+  DevInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* lse2 = static_cast<float*>(workspace);
+  float* delta = lse2 + (size_t)H * Tq;
+  if (Tq > 0 && fa::launch_bwd_prep(o, dout, lse, lse2, delta, (int)Tq, H, D, varlen ? 1 : Sq, varlen ? 1 : 0,
+                                    dtype == FA_FP16 ? 1 : 0, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  const CUtensorMapDataType dt = dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t cols = (uint64_t)H * D;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((st = make_map(&mq, q, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&mk, k, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&mv, v, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&mdo, dout, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
+  for (int dir = 0; dir < 2; ++dir) {   // 0: dK, dV;  1: dQ
+    fa::BwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const bool dqk = dir == 1;
+    L.tr1 = dqk ? mq : mk;
+    L.tr2 = dqk ? mdo : mv;
+    L.tt1 = dqk ? mk : mq;
+    L.tt2 = dqk ? mv : mdo;
+    L.p.dr1 = dqk ? dq : dk;
+    L.p.dr2 = dqk ? nullptr : dv;
+    L.p.lse2 = lse2;
+    L.p.delta = delta;
+    L.p.cu_q = cu_seqlens_q;
+    L.p.cu_k = cu_seqlens_k;
+    L.p.B = B;
+    L.p.H = H;
+    L.p.Sq = Sq;
+    L.p.Sk = Sk;
+    L.p.total_q = (int)Tq;
+    L.p.total_k = (int)Tk;
+    L.p.n_rblk = (int)(dqk ? nq : nk);
+    L.p.ntiles = B * H * L.p.n_rblk;
+    L.p.c = (float)((double)scale * 1.4426950408889634);
+    L.p.scale = scale;
+    L.p.status = dev->status;
+    L.p.sched = dev->take_slot();
+    L.D = D;
+    L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
+    L.causal = causal != 0;
+    L.dq = dqk;
+    L.num_sms = dev->sms;
+    L.stream = s;
+    if (L.p.ntiles == 0) continue;
+    const cudaError_t e = D == 64 ? fa::launch_bwd_d64(L) : fa::launch_bwd_d128(L);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+  }
+  return FA_OK;
 }
 
 int fa_get_device_status(void* stream, int* raw) {

@@ -75,6 +75,46 @@ cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, voi
 cudaError_t launch_fwd_fp8_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
 
+// Backward pass. Both kernels are one template in two orientations: a
+// 128-row block of the "resident" side (R1, R2) stays in shared memory while
+// 128-row blocks of the "streamed" side (T1, T2) pass through.
+//   dQ kernel:   R1 = Q, R2 = dO, T1 = K, T2 = V   -> dr1 = dQ
+//   dK/dV kernel: R1 = K, R2 = V, T1 = Q, T2 = dO  -> dr1 = dK, dr2 = dV
+struct BwdParams {
+  void* dr1;               // [tokens_R, H, D] gradient of the resident side, input type
+  void* dr2;               // dV (dK/dV kernel), else nullptr
+  const float* lse2;       // [H, total_q]: LSE * log2(e), +inf for rows with no key
+  const float* delta;      // [H, total_q]: rowsum(dO * O)
+  const int* cu_q;         // varlen prefix sums [B + 1] (device) or nullptr
+  const int* cu_k;
+  int B, H, Sq, Sk;        // fixed lengths, or (varlen) max lengths
+  int total_q, total_k;
+  int n_rblk;              // resident 128-row blocks per (sequence, head)
+  int ntiles;              // B * H * n_rblk
+  float c;                 // softmax scale * log2(e)
+  float scale;             // softmax scale (the factor of dQ and dK)
+  int* status;
+  unsigned int* sched;
+};
+
+struct BwdLaunch {
+  CUtensorMap tr1, tr2, tt1, tt2;
+  BwdParams p;
+  int D;
+  int kind;  // kF16 or kBF16
+  bool causal;
+  bool dq;   // true: dQ kernel, false: dK/dV kernel
+  int num_sms;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_bwd_d64(const BwdLaunch& L);
+cudaError_t launch_bwd_d128(const BwdLaunch& L);
+// lse2 / delta of every (query token, head) from O, dO and the forward's LSE
+// (lse_varlen: LSE is [H, total_q], else [B, H, Sq])
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* delta,
+                            int total_q, int H, int D, int Sq, int lse_varlen, int fp16, cudaStream_t stream);
+
 // FP8 preparation: rotation (optional) + block quantisation of one tensor.
 struct PrepParams {
   const void* x;        // [tokens, H, D] 16-bit input

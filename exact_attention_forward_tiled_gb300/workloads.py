@@ -31,6 +31,7 @@ class Workload:
     len_range: tuple = (128, 8192)   # varlen: inclusive uniform range of lengths
     outliers: bool = False           # fp8 outlier workload
     splitkv: bool = False            # run through the split-KV forward
+    backward: bool = False           # forward + backward step (an upstream gradient dO is drawn too)
     note: str = field(default="", compare=False)
 
 
@@ -53,6 +54,11 @@ WORKLOADS = {
     # = 16 work tiles alone would leave most SMs idle
     "f1": Workload("bf16_splitkv_B2_H8_Sq256_Sk65536_D128", "bf16", 2, 8, 256, 65536, 128, False, 6,
                    splitkv=True, note="bf16 split-KV B=2 H=8 Sq=256 Sk=65536 D=128 non-causal"),
+    # backward: the forward's shapes with an upstream gradient dO ~ N(0, 1)
+    "b1": Workload("bf16_bwd_B4_H16_S8192_D128", "bf16", 4, 16, 8192, 8192, 128, False, 7, backward=True,
+                   note="bf16 backward B=4 H=16 Sq=Sk=8192 D=128 non-causal"),
+    "b2": Workload("bf16_bwd_causal_B2_H16_S16384_D128", "bf16", 2, 16, 16384, 16384, 128, True, 8,
+                   backward=True, note="bf16 backward causal B=2 H=16 Sq=Sk=16384 D=128"),
 }
 
 TORCH_DTYPE = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
@@ -84,7 +90,7 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
 
     Returns a dict with q, k, v, cu_seqlens_q/k (None unless varlen), the
     lengths and, for the FP8 workload, sigma (int8 +-1 of length D) and the
-    outlier columns. Random numbers come from a ``torch.Generator`` on
+    outlier columns; for a backward workload also dO (drawn after V). Random numbers come from a ``torch.Generator`` on
     ``device`` seeded with the workload's seed.
     """
     seed = w.seed if seed is None else seed
@@ -123,6 +129,8 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
         sig = torch.randint(0, 2, (w.D,), generator=g, device=device, dtype=torch.int32) * 2 - 1
         out["sigma"] = sig.to(torch.int8)
     out["q"], out["k"], out["v"] = q.to(dt), k.to(dt), v.to(dt)
+    if w.backward:
+        out["do"] = torch.randn((Tq, w.H, w.D), generator=g, device=device, dtype=torch.float32).to(dt)
     return out
 
 

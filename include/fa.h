@@ -237,6 +237,44 @@ int fa_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
                       float scale, int causal, void* stream);
 
 /*
+ * fa_bwd_workspace_size -- bytes of device scratch fa_bwd needs: two fp32
+ * values per (query token, head), rounded up to 256. 0 when there is nothing
+ * to do.
+ */
+size_t fa_bwd_workspace_size(int H, int total_q);
+
+/*
+ * fa_bwd -- gradients of fa_fwd: dQ, dK, dV for an upstream gradient dO.
+ *
+ * The pages define the forward only ("Flash Attention 3 principles
+ * (guijiagi)" section 1.2 with the section 2.2 softmax; the FlashAttention-3
+ * wiki's table reports the backward's speed). This is the exact derivative of
+ * that forward, with P recomputed from the forward's LSE:
+ *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),  dQ = scale dS K,
+ *   dK = scale dS^T Q.
+ *
+ *   q, k, v, o   the forward's inputs and output, layouts as fa_fwd
+ *   dout         dO, same shape and type as o
+ *   lse          the forward's LSE (fp32, [B, H, Sq] or varlen [H, total_q])
+ *   dq, dk, dv   outputs, shapes and type of q, k, v (written; every row of
+ *                every sequence, 0 where no pair is visible)
+ *   B..dtype     as fa_fwd; D = 64 or 128 (256 -> FA_ERR_UNSUPPORTED)
+ *   workspace    device scratch of at least fa_bwd_workspace_size(H, total_q)
+ *                bytes, 256-byte aligned; holds the per-row constants
+ *
+ * P and dS are rounded to the input type before they enter the tensor-core
+ * products (as P is in the forward); accumulation is fp32. Deterministic: no
+ * atomics, every output row is written by one CTA. Three kernels on `stream`
+ * (row constants, dK/dV, dQ). Bad varlen sequences are skipped and reported
+ * as FA_ERR_DEVICE_SEQLENS by fa_get_device_status.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D,
+           float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+           int total_q, int total_k, void* workspace, size_t workspace_bytes, int dtype,
+           void* stream);
+
+/*
  * fa_get_device_status -- synchronise `stream`, then read and clear the
  * current device's status word. Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a
  * kernel's bounded wait expired; the kernel left early and its outputs are
