@@ -25,7 +25,10 @@
 //
 // Roles: eight "softmax" warps (two warpgroups, each owning half of the 128
 // streamed columns of every resident row: thread = resident row), one MMA
-// warp (one thread issues), one load warp (TMA). Every mbarrier wait is
+// warp (one thread issues), one load warp (TMA). The softmax warps hand a
+// block back in two phases -- P as soon as S is read, dS once dP is -- and
+// the MMA warp fills the gaps with the next block's S and dP products, so the
+// tensor core keeps working while P and dS are made. Every mbarrier wait is
 // bounded (see pipeline.cuh).
 #pragma once
 
@@ -65,10 +68,15 @@ struct BwdCfg {
   static constexpr int kVecBytes = 2 * 64 * 4;                   // -lse2[64], -delta[64]
   static constexpr int kOffBar = kOffVec + kSoftmaxWarps * kVecBytes;
   static constexpr int kTileRing = 4;
+  // barriers: r_full, r_empty, t_full[S], t_empty[S]; x_full, y_full (MMA ->
+  // softmax: S or dP of the block is in tensor memory); p_full, ds_full
+  // (softmax -> MMA: P, then dS, of the block handed back); acc_full,
+  // mma_done, tile_full[R], tile_empty[R]
   static constexpr int kBarRFull = 0, kBarREmpty = 1, kBarTFull = 2, kBarTEmpty = 2 + STAGES,
-                       kBarSFull = 2 + 2 * STAGES, kBarZFull = kBarSFull + 1, kBarAccFull = kBarZFull + 1,
-                       kBarMmaDone = kBarAccFull + 1, kBarTileFull = kBarMmaDone + 1,
-                       kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
+                       kBarXFull = 2 + 2 * STAGES, kBarYFull = kBarXFull + 1, kBarPFull = kBarYFull + 1,
+                       kBarDSFull = kBarPFull + 1, kBarAccFull = kBarDSFull + 1, kBarMmaDone = kBarAccFull + 1,
+                       kBarTileFull = kBarMmaDone + 1, kBarTileEmpty = kBarTileFull + kTileRing,
+                       kNumBars = kBarTileEmpty + kTileRing;
   static constexpr int kTileConsumers = 1 + kSoftmaxWarps;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
@@ -178,7 +186,7 @@ __device__ void bwd_load_role(const CUtensorMap* tr1, const CUtensorMap* tr2, co
 
   for (int j = 0; ok; ++j) {
     const int rs = j % C::kTileRing;
-    if (!wt.wait(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 29)) break;
+    if (!wt.wait(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 20)) break;
     const int w = bwd_fetch_tile(p, j);
     ring.slots[rs] = w;
     ptx::mbar_arrive(ring.full(rs));
@@ -215,14 +223,15 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
   const uint32_t r1 = sbase + C::kOffR, r2 = r1 + C::kTileBytes;
   auto slot_addr = [&](uint32_t c) { return sbase + C::kOffT + (c % C::STAGES) * C::kTileBytes; };
 
-  // X or Y = R T^T over the head dimension (both K-major)
-  auto mm_s = [&](uint32_t col, uint32_t r_addr, uint32_t t_addr) {
+  // X or Y = R T^T over the head dimension (both K-major), committed to `b`
+  auto mm_s = [&](uint32_t col, uint32_t r_addr, uint32_t t_addr, int b) {
 #pragma unroll
     for (int kk = 0; kk < C::kKSteps; ++kk) {
       const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
       ptx::mma_f16_ss(tmem + col, ptx::smem_desc_sw128(r_addr + off, 16, 1024),
                       ptx::smem_desc_sw128(t_addr + off, 16, 1024), idesc_s, kk > 0);
     }
+    ptx::mma_commit(bar(b));
   };
   // acc (+)= Z T: Z (16-bit, in tensor memory over X or Y; warpgroup g's 64
   // streamed rows packed at columns 64 g .. 64 g + 31) times the T tile
@@ -241,6 +250,13 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
     return r;
   };
 
+  // Issue order per block i (T tiles of block i in slots c, c + 1):
+  //   [P_i handed back]  dV += P_i^T dO_i (dK/dV kernel),  X_{i+1}
+  //   [dS_i handed back] acc1 += dS_i T1_i,                Y_{i+1}
+  // so the tensor core computes the next block's scores while the softmax
+  // warps turn this block's dP into dS, and the next block's dP while they
+  // make the next P. X_{i+1} overwrites P_i and Y_{i+1} overwrites dS_i only
+  // after the products that read them (tcgen05 MMAs run in issue order).
   uint32_t tc = 0, it = 0, rcount = 0;
   bool ok = true;
   int w = 0;
@@ -250,24 +266,35 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
     if (!(ok = wt.wait(bar(C::kBarRFull), rcount & 1u, 24))) break;
     ++rcount;
     ptx::tc_fence_after();
-    for (int i = 0; i < ti.n_t; ++i, ++it) {
-      const uint32_t c1 = tc, c2 = tc + 1;
-      tc += 2;
-      if (!(ok = t_ready(c1))) break;
-      mm_s(C::kColX, r1, slot_addr(c1));
-      if (!(ok = t_ready(c2))) break;
-      mm_s(C::kColY, r2, slot_addr(c2));
-      ptx::mma_commit(bar(C::kBarSFull));
-      if (i == ti.n_t - 1) ptx::mma_commit(bar(C::kBarREmpty));   // last use of R1, R2
-      if (!(ok = wt.wait(bar(C::kBarZFull), it & 1u, 25))) break;
+    const int n = ti.n_t;
+    if (!(ok = t_ready(tc))) break;
+    mm_s(C::kColX, r1, slot_addr(tc), C::kBarXFull);
+    if (!(ok = t_ready(tc + 1))) break;
+    mm_s(C::kColY, r2, slot_addr(tc + 1), C::kBarYFull);
+    if (n == 1) ptx::mma_commit(bar(C::kBarREmpty));   // last use of R1, R2
+    for (int i = 0; i < n; ++i, ++it) {
+      const uint32_t c = tc + 2 * i;
+      const bool more = i + 1 < n;
+      if (!(ok = wt.wait(bar(C::kBarPFull), it & 1u, 25))) break;
       ptx::tc_fence_after();
-      // dQ kernel: dQ += dS K.  dK/dV kernel: dK += dS^T Q, dV += P^T dO
-      mm_acc(C::kColAcc1, C::kColY, slot_addr(c1), i > 0);
-      if (!C::DQ) mm_acc(C::kColAcc2, C::kColX, slot_addr(c2), i > 0);
-      ptx::mma_commit(bar(C::kBarTEmpty + (int)(c1 % C::STAGES)));
-      ptx::mma_commit(bar(C::kBarTEmpty + (int)(c2 % C::STAGES)));
+      if (!C::DQ) mm_acc(C::kColAcc2, C::kColX, slot_addr(c + 1), i > 0);   // dV += P^T dO
+      if (more) {
+        if (!(ok = t_ready(c + 2))) break;
+        mm_s(C::kColX, r1, slot_addr(c + 2), C::kBarXFull);
+      }
+      if (!(ok = wt.wait(bar(C::kBarDSFull), it & 1u, 26))) break;
+      ptx::tc_fence_after();
+      mm_acc(C::kColAcc1, C::kColY, slot_addr(c), i > 0);   // dQ += dS K  or  dK += dS^T Q
+      ptx::mma_commit(bar(C::kBarTEmpty + (int)(c % C::STAGES)));
+      ptx::mma_commit(bar(C::kBarTEmpty + (int)((c + 1) % C::STAGES)));
+      if (more) {
+        if (!(ok = t_ready(c + 3))) break;
+        mm_s(C::kColY, r2, slot_addr(c + 3), C::kBarYFull);
+        if (i + 2 == n) ptx::mma_commit(bar(C::kBarREmpty));
+      }
     }
     if (!ok) break;
+    tc += 2 * n;
     ptx::mma_commit(bar(C::kBarAccFull));
   }
   ptx::mma_commit(bar(C::kBarMmaDone));
@@ -373,8 +400,6 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
         }
         __syncwarp();
       }
-      if (!(ok = wt.wait_warp(bar(C::kBarSFull), it & 1u, 26))) break;
-      ptx::tc_fence_after();
       // visible columns of this thread: [lo, hi) relative to col0
       int lo, hi;
       if (C::DQ) {
@@ -384,30 +409,29 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
         lo = q_lo - col0;
         hi = row_ok ? ti.Lq - col0 : 0;
       }
-      // two chunks of 32 columns; chunk ch's 16-bit results go to columns
-      // 64 g + 16 ch, which this warpgroup has already read
+      // phase 1: P = exp2(S c - lse2) of this warpgroup's 64 columns, kept in
+      // registers; the dK/dV kernel also stores it (16-bit, columns 64 g ..
+      // 64 g + 31, already read) for dV += P^T dO. The hand-off also tells
+      // the MMA warp that S has been read.
+      if (!(ok = wt.wait_warp(bar(C::kBarXFull), it & 1u, 27))) break;
+      ptx::tc_fence_after();
+      float pv[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t xv[32], yv[32];
+        uint32_t xv[32];
         ptx::tmem_ld32(tl + C::kColX + 64 * g + 32 * ch, xv);
-        ptx::tmem_ld32(tl + C::kColY + 64 * g + 32 * ch, yv);
         ptx::tmem_wait_ld();
         ptx::reg_fence(xv);
-        ptx::reg_fence(yv);
         const int clo = lo - 32 * ch, chi = hi - 32 * ch;
         const bool masked = clo > 0 || chi < 32;
-        uint32_t pk_p[16], pk_ds[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          uint64_t nl2, nd2;
+          uint64_t nl2;
           if (C::DQ) {
             nl2 = ptx::f2pack(nl_row, nl_row);
-            nd2 = ptx::f2pack(nd_row, nd_row);
           } else {
             const float2 a = *reinterpret_cast<const float2*>(vec + 32 * ch + j);
-            const float2 b = *reinterpret_cast<const float2*>(vec + 64 + 32 * ch + j);
             nl2 = ptx::f2pack(a.x, a.y);
-            nd2 = ptx::f2pack(b.x, b.y);
           }
           float e0, e1;
           ptx::f2unpack(ptx::fma2(ptx::f2pack(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1])), c2, nl2),
@@ -417,22 +441,53 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
             p0 = (j >= clo && j < chi) ? p0 : 0.f;
             p1 = (j + 1 >= clo && j + 1 < chi) ? p1 : 0.f;
           }
+          pv[32 * ch + j] = p0;
+          pv[32 * ch + j + 1] = p1;
+        }
+        if (!C::DQ) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack16<C::KIND>(pv[32 * ch + 2 * j], pv[32 * ch + 2 * j + 1]);
+          ptx::tmem_st16(tl + C::kColX + 64 * g + 16 * ch, pk);
+        }
+      }
+      if (!C::DQ) ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull));
+      // phase 2: dS = P (dP - Delta), 16-bit, over dP (columns 64 g .. 64 g + 31)
+      if (!(ok = wt.wait_warp(bar(C::kBarYFull), it & 1u, 28))) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t yv[32];
+        ptx::tmem_ld32(tl + C::kColY + 64 * g + 32 * ch, yv);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(yv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          uint64_t nd2;
+          if (C::DQ) {
+            nd2 = ptx::f2pack(nd_row, nd_row);
+          } else {
+            const float2 b = *reinterpret_cast<const float2*>(vec + 64 + 32 * ch + j);
+            nd2 = ptx::f2pack(b.x, b.y);
+          }
           const uint64_t t = ptx::add2(ptx::f2pack(__uint_as_float(yv[j]), __uint_as_float(yv[j + 1])), nd2);
           float d0, d1;
-          ptx::f2unpack(ptx::mul2(ptx::f2pack(p0, p1), t), d0, d1);
-          pk_p[j >> 1] = pack16<C::KIND>(p0, p1);
-          pk_ds[j >> 1] = pack16<C::KIND>(d0, d1);
+          ptx::f2unpack(ptx::mul2(ptx::f2pack(pv[32 * ch + j], pv[32 * ch + j + 1]), t), d0, d1);
+          pk[j >> 1] = pack16<C::KIND>(d0, d1);
         }
-        if (!C::DQ) ptx::tmem_st16(tl + C::kColX + 64 * g + 16 * ch, pk_p);
-        ptx::tmem_st16(tl + C::kColY + 64 * g + 16 * ch, pk_ds);
+        ptx::tmem_st16(tl + C::kColY + 64 * g + 16 * ch, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarZFull));
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarDSFull));
     }
     if (!ok) return;
-    if (!wt.wait_warp(bar(C::kBarAccFull), acount & 1u, 27)) return;
+    if (!wt.wait_warp(bar(C::kBarAccFull), acount & 1u, 29)) return;
     ++acount;
     ptx::tc_fence_after();
     if (C::DQ) {
@@ -442,8 +497,8 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
     } else {
       store_acc_row<C::KIND>(tl + C::kColAcc2, C::D, 1.f, out2, row_ok);       // dV
     }
-    // the next tile's first accumulating MMA overwrites these columns only
-    // after this warp's next Z hand-off
+    // the next tile's first accumulating MMAs overwrite these columns only
+    // after this warp's next P and dS hand-offs
     ptx::tc_fence_before();
   }
 }
@@ -467,7 +522,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t bars = sbase + C::kOffBar;
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
-      if (i == C::kBarZFull) count = C::kSoftmaxWarps;
+      if (i == C::kBarPFull || i == C::kBarDSFull) count = C::kSoftmaxWarps;
       if (i >= C::kBarTileEmpty) count = C::kTileConsumers;
       ptx::mbar_init(bars + 8u * i, count);
     }
