@@ -2,5 +2,5 @@
 #include "bwd_kernel.cuh"
 
 namespace fa {
-cudaError_t launch_bwd_d64(const BwdLaunch& L) { return launch_bwd_impl<64, 8>(L); }
+cudaError_t launch_bwd_d64(const BwdLaunch& L) { return launch_bwd_impl<64, 8, 8>(L); }
 }  // namespace fa

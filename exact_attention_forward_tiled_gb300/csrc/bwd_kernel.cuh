@@ -65,7 +65,7 @@ struct BwdCfg {
   static constexpr int kOffR = 0;                                // R1, R2
   static constexpr int kOffT = 2 * kTileBytes;                   // ring of T tiles
   static constexpr int kOffVec = kOffT + STAGES * kTileBytes;    // per-warp column constants
-  static constexpr int kVecBytes = 2 * 64 * 4;                   // -lse2[64], -delta[64]
+  static constexpr int kVecBytes = DQ ? 0 : 2 * 64 * 4;
   static constexpr int kOffBar = kOffVec + kSoftmaxWarps * kVecBytes;
   static constexpr int kTileRing = 4;
   // barriers: r_full, r_empty, t_full[S], t_empty[S]; x_full, y_full (MMA ->
@@ -581,11 +581,11 @@ cudaError_t launch_bwd_dir(const BwdLaunch& L) {
   return cudaGetLastError();
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES_KV, int STAGES_Q>
 cudaError_t launch_bwd_impl(const BwdLaunch& L) {
   if (L.kind == kF16)
-    return L.dq ? launch_bwd_dir<D, STAGES, kF16, true>(L) : launch_bwd_dir<D, STAGES, kF16, false>(L);
-  return L.dq ? launch_bwd_dir<D, STAGES, kBF16, true>(L) : launch_bwd_dir<D, STAGES, kBF16, false>(L);
+    return L.dq ? launch_bwd_dir<D, STAGES_Q, kF16, true>(L) : launch_bwd_dir<D, STAGES_KV, kF16, false>(L);
+  return L.dq ? launch_bwd_dir<D, STAGES_Q, kBF16, true>(L) : launch_bwd_dir<D, STAGES_KV, kBF16, false>(L);
 }
 
 }  // namespace fa
