@@ -15,6 +15,10 @@ the outputs copied back inside the timed region. ``roofline`` compares the
 kernel with the measured dense bf16 tensor-core peak; ``cpu_baseline`` times
 the fp64 oracle on the host cores on a bounded sample of the same workload.
 
+Paged workloads (``--workload p1`` / ``p2``): one ``fa_fwd_paged`` call over a
+K/V cache of shuffled 16-key pages (p2, decode, with automatic key ranges and
+an HBM roofline: one read of the cache).
+
 Backward workloads (``--workload b1`` / ``b2``): a step is one ``fa_bwd``
 call (row constants, dK/dV kernel, dQ kernel) for O, LSE from one forward run
 before timing; the metric counts 2.5x the forward's FLOPs (the five matrix
@@ -164,24 +168,24 @@ def oracle_sample(w, inputs, seconds=10.0, max_rows=None):
     import numpy as np
     if w.varlen:
         cu = inputs["cu_seqlens_q"].cpu().tolist()
-        bounds = [(cu[b], cu[b + 1]) for b in range(w.B)]
+        bounds = [((cu[b], cu[b + 1]), (cu[b], cu[b + 1])) for b in range(w.B)]
     else:
-        bounds = [(b * w.Sq, (b + 1) * w.Sq) for b in range(w.B)]
+        bounds = [((b * w.Sq, (b + 1) * w.Sq), (b * w.Sk, (b + 1) * w.Sk)) for b in range(w.B)]
     scale = w.D ** -0.5
     spent, pairs, rows, heads = 0.0, 0, 0, 0
-    for b, (s0, s1) in enumerate(bounds):
+    for b, ((s0, s1), (k0, k1)) in enumerate(bounds):
         for h in range(w.H):
             L = s1 - s0
             if L == 0:
                 continue
             q = orc._f64(inputs["q"][s0:s1, h, :])
-            k = orc._f64(inputs["k"][s0:s1, h, :])
-            v = orc._f64(inputs["v"][s0:s1, h, :])
+            k = orc._f64(inputs["k"][k0:k1, h, :])
+            v = orc._f64(inputs["v"][k0:k1, h, :])
             pos = np.arange(L) if max_rows is None else np.arange(min(L, max_rows))
             t0 = time.perf_counter()
             orc.attention_head(q[pos], pos, k, v, L, scale, w.causal)
             spent += time.perf_counter() - t0
-            pairs += orc.visible_pairs(pos, L, L, w.causal)
+            pairs += orc.visible_pairs(pos, k1 - k0, L, w.causal)
             rows += len(pos)
             heads += 1
             if spent >= seconds or max_rows is not None:
@@ -350,6 +354,8 @@ def main(argv=None):
         lse = torch.empty((w.B, w.H, w.Sq), device=dev, dtype=torch.float32)
         Sq, Sk = w.Sq, w.Sk
         flops = A.attention_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
+        if w.Sq != w.Sk:   # count the visible pairs exactly (bottom-right causal mask)
+            flops = A.visible_pair_flops(w.H, w.D, [w.Sq] * w.B, [w.Sk] * w.B, w.causal)
         extra = {}
 
     # one step = the whole hot path; for fp8 the prep kernel then the attention;
@@ -371,6 +377,20 @@ def main(argv=None):
             return [lambda: api.fa_bwd(*i_, *o_, w.B, w.H, Sq, Sk, w.D, scale, w.causal, workspace=bwd_ws,
                                        workspace_bytes=ws_bytes, stream=st)]
         names = ["fa_bwd (bwd_prep_kernel + fa_bwd_kernel dK/dV + fa_bwd_kernel dQ)"]
+    elif w.page_size:
+        kc, vc, table, seqlens = (inputs[n] for n in ("k_cache", "v_cache", "block_table", "seqlens_k"))
+        max_pages = table.shape[1]
+        splits = 0 if w.Sq == 1 else 1   # decode: automatic key ranges
+        ws_bytes = (api.fa_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, max_pages * w.page_size, w.D, splits)
+                    if splits != 1 else 0)
+        paged_ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        ins = [q]   # the K/V cache stays resident on the device, as in serving
+
+        def hot_path(i_, o_, st):
+            return [lambda: api.fa_fwd_paged(i_[0], kc, vc, table, seqlens, *o_, w.B, w.H, w.Sq, w.D, kc.shape[0],
+                                             w.page_size, max_pages, scale, w.causal, splits, paged_ws, ws_bytes,
+                                             stream=st)]
+        names = ["fa_fwd_kernel (paged)" + (" + splitkv_merge_kernel" if splits != 1 else "")]
     elif fp8:
         prep = api.fp8_prepare(q, k, v, inputs["sigma"], batch=w.B, stream=stream)
 
@@ -508,7 +528,7 @@ def main(argv=None):
         kern = "fa_bwd"
         peak_note += ("; achieved = algorithmic backward FLOPs (5 matrix products, 2.5x the forward's) over "
                       "the whole fa_bwd call (3 kernels; the dQ kernel recomputes S and dP, 7 products run)")
-    if w.splitkv:
+    if w.splitkv or (w.page_size and w.Sq == 1):
         peak_note += "; achieved covers the attention and the merge kernel of each call"
     line = {
         "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -531,11 +551,23 @@ def main(argv=None):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "note": ("pinned host -> device copy of Q, K, V, O, LSE, dO and device -> host copy of dQ, "
                          "dK, dV every step" if w.backward else
+                         "pinned host -> device copy of Q and device -> host copy of O, LSE every step; the "
+                         "paged K/V cache stays resident" if w.page_size else
                          "pinned host -> device copy of Q, K, V and device -> host copy of O, LSE every step")
                         + "; copies of neighbouring steps overlap compute (two buffer sets, H2D / D2H streams)"},
-        "gpu_launches": args.steps * (3 if w.backward else 2 if w.splitkv else len(kernels)),
+        "gpu_launches": args.steps * (3 if w.backward else 2 if (w.splitkv or (w.page_size and w.Sq == 1))
+                                      else len(kernels)),
         "clocks": clk.summary(),
     }
+    if w.page_size and w.Sq == 1:
+        # decode: one query per sequence; the bound is reading the cache once
+        kvb = A.paged_kv_bytes(w.H, w.D, [w.Sk] * w.B)
+        gbs = kvb / (attn_ms * 1e-3) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(kern, w.name),
+                            "peak_source": f"{peak_src} HBM copy bandwidth, MEASURED_PEAKS.json; achieved = one "
+                                           "read of every cached K and V row over the attention + merge call",
+                            "kernel": kern, "kernel_ms": attn_ms, "bytes": kvb}
     if fp8:
         pb = A.prep_bytes(w.H, w.D, w.B, w.Sq)
         gbs = pb / (per_kernel[0] * 1e-3) / 1e9

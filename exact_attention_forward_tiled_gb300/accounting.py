@@ -22,6 +22,27 @@ def attention_flops(H, D, lengths_q, lengths_k, causal) -> float:
     return total
 
 
+def visible_pair_flops(H, D, lengths_q, lengths_k, causal) -> float:
+    """Forward FLOPs counted exactly, 4 * D per visible (query, key) pair, for
+    workloads where Sq != Sk under the causal mask (bottom-right aligned:
+    query i of Lq sees keys j <= i + Lk - Lq)."""
+    total = 0
+    for lq, lk in zip(lengths_q, lengths_k):
+        if not causal:
+            total += lq * lk
+            continue
+        # sum over i of clamp(i + lk - lq + 1, 0, lk)
+        for i in range(lq):
+            total += max(0, min(lk, i + lk - lq + 1))
+    return 4.0 * H * D * total
+
+
+def paged_kv_bytes(H, D, lengths_k, elem_bytes=2) -> float:
+    """Algorithmic HBM bytes of a decode step over a paged cache: one read of
+    every key and value row of every sequence."""
+    return 2.0 * H * D * elem_bytes * sum(lengths_k)
+
+
 def attention_bwd_flops(H, D, lengths_q, lengths_k, causal) -> float:
     """Backward FLOPs by the usual convention: five matrix products of
     2 * Sq * Sk * D each (S, dP, dV, dK, dQ), i.e. 2.5x the forward's, halved

@@ -115,7 +115,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
-int fa_version(void) { return (1 << 16) | 2; }
+int fa_version(void) { return (1 << 16) | 3; }
 
 const char* fa_strerror(int s) {
   switch (s) {
@@ -288,6 +288,72 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   if (st != FA_OK || nothing) return st;
   int n = 1, per = 1;
   resolve_splits(B, H, Sq, Sk, D, num_splits, dev->sms, &n, &per);
+  const size_t need = splitkv_bytes(B, H, Sq, D, n);
+  if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  const int64_t ntiles = (int64_t)L.p.ntiles * n;
+  if (ntiles > INT32_MAX) return FA_ERR_INVALID_ARG;
+  L.p.ntiles = (int)ntiles;
+  L.p.n_split = n;
+  L.p.split_blocks = per;
+  L.p.o_part = static_cast<float*>(workspace);
+  L.p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          round256((size_t)n * B * Sq * H * D * sizeof(float)));
+  if ((st = launch16(L, dev)) != FA_OK) return st;
+  cudaError_t e = fa::launch_splitkv_merge(L.p.o_part, L.p.lse_part, o, lse, n, B, H, Sq, D,
+                                           dtype == FA_FP16, L.stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                 const int* seqlens_k, void* o, float* lse, int B, int H, int Sq, int D, int num_pages,
+                 int page_size, int max_pages, float scale, int causal, int num_splits, void* workspace,
+                 size_t workspace_bytes, int dtype, void* stream) {
+  // ---- host-side checks of the paging arguments (the rest: setup_fwd16)
+  if (num_pages <= 0 || max_pages <= 0 || B < 0) return FA_ERR_INVALID_ARG;
+  if (!(page_size == 16 || page_size == 32 || page_size == 64 || (page_size > 0 && page_size % 128 == 0)))
+    return FA_ERR_INVALID_ARG;
+  if ((int64_t)num_pages * page_size + 128 > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)max_pages * page_size > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)B * max_pages > INT32_MAX) return FA_ERR_INVALID_ARG;
+  const int Sk = max_pages * page_size;   // the most keys a sequence can have
+  if (B > 0 && (!block_table || !seqlens_k)) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_table) & 3u || reinterpret_cast<uintptr_t>(seqlens_k) & 3u)
+    return FA_ERR_ALIGNMENT;
+  fa::FwdLaunch L;
+  DevInfo* dev = nullptr;
+  bool nothing = false;
+  // the contiguous setup with K/V as one sequence of rows; the K/V maps are
+  // replaced below by maps over the whole caches
+  int st = setup_fwd16(L, &dev, &nothing, q, k_cache, v_cache, o, lse, B, H, Sq, 0, D, scale, causal, nullptr,
+                       nullptr, 0, 0, dtype, stream);
+  if (st != FA_OK || nothing) return st;
+  const CUtensorMapDataType dt = dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t cols = (uint64_t)H * D, rows = (uint64_t)num_pages * page_size;
+  const uint32_t box_rows = page_size < 128 ? (uint32_t)page_size : 128u;
+  if ((st = make_map(&L.tk, k_cache, dt, 2, cols, rows, 64, box_rows)) != FA_OK) return st;
+  if ((st = make_map(&L.tv, v_cache, dt, 2, cols, rows, 64, box_rows)) != FA_OK) return st;
+  L.p.Sk = Sk;
+  L.p.total_k = (int)rows;
+  L.p.block_table = block_table;
+  L.p.seqlens_k = seqlens_k;
+  L.p.max_pages = max_pages;
+  L.p.page_size = page_size;
+  L.p.num_pages = num_pages;
+  L.p.page_rows = (int)box_rows;
+  L.p.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
+  int n = 1, per = 1;
+  resolve_splits(B, H, Sq, Sk, D, num_splits, dev->sms, &n, &per);
+  if (num_splits == 1) n = 1;
+  if (n == 1) {
+    L.p.split_blocks = 1 << 30;
+    return launch16(L, dev);
+  }
   const size_t need = splitkv_bytes(B, H, Sq, D, n);
   if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;

@@ -48,6 +48,15 @@ struct FwdParams {
   // scales are then [cu_blocks[B], H] (nullptr: fixed length, [B, H, nblk])
   const int* cu_blocks_q;
   const int* cu_blocks_k;
+  // paged K/V (block_table == nullptr: contiguous). The K and V tensor maps
+  // cover the caches as [num_pages * page_size, H * D] rows; key j of
+  // sequence b is row block_table[b * max_pages + j / page_size] * page_size
+  // + j % page_size. seqlens_k [B]: keys of each sequence. page_rows =
+  // min(page_size, 128) rows per TMA box.
+  const int* block_table;
+  const int* seqlens_k;
+  int max_pages, page_size, num_pages, page_rows;
+  int page_shift;   // log2(page_size) for a power of two, else -1
 };
 
 // Element kinds of the attention inputs.

@@ -147,7 +147,18 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   t.qblk = qblk;
   t.b = bh / p.H;
   t.h = bh - t.b * p.H;
-  if (p.cu_q != nullptr) {
+  if (p.block_table != nullptr) {
+    // paged K/V: fixed query length, keys from seqlens_k through the block table
+    t.qtok = t.b * p.Sq;
+    t.ktok = 0;
+    t.Lq = p.Sq;
+    t.Lk = __ldg(p.seqlens_k + t.b);
+    if (t.Lk < 0 || t.Lk > p.Sk) {
+      t.Lq = 0;
+      t.Lk = 0;
+      if (qblk == 0) atomicOr(p.status, kDevBadSeqlens);
+    }
+  } else if (p.cu_q != nullptr) {
     const int qs = __ldg(p.cu_q + t.b), qe = __ldg(p.cu_q + t.b + 1);
     const int ks = __ldg(p.cu_k + t.b), ke = __ldg(p.cu_k + t.b + 1);
     t.qtok = qs;
@@ -213,12 +224,69 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     for (int bx = 0; bx < C::kBoxes; ++bx)
       ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
   };
-  auto load_kv = [&](const CUtensorMap* m, int h, int row) -> bool {
+  // paged K/V: rows of the (up to 8) page_rows-row boxes of one 128-key
+  // block, looked up once per block (K and V share them). page_fetch issues
+  // the block-table reads before the caller waits for a free slot, and
+  // page_rows computes the rows after it, so the table's load latency hides
+  // behind the wait. Page sizes that are powers of two divide by shifting.
+  int rows_b = -1, rows_kb = -1, fetched_b = -1, fetched_kb = -1;
+  int prow[8];
+  auto page_fetch = [&](const TileInfo& ti, int kb) {
+    if ((ti.b == rows_b && kb == rows_kb) || (ti.b == fetched_b && kb == fetched_kb)) return;
+    fetched_b = ti.b;
+    fetched_kb = kb;
+    const int nsub = 128 / p.page_rows;
+    const int* tab = p.block_table + (int64_t)ti.b * p.max_pages;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int key = 128 * kb + s * p.page_rows;
+      const int pi = p.page_shift >= 0 ? key >> p.page_shift : key / p.page_size;
+      prow[s] = (s < nsub && key < ti.Lk) ? __ldg(tab + pi) : -2;   // -2: a box past the sequence
+    }
+  };
+  auto page_rows = [&](int kb) {
+    if (fetched_b == rows_b && fetched_kb == rows_kb) return;
+    rows_b = fetched_b;
+    rows_kb = fetched_kb;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int key = 128 * kb + s * p.page_rows;
+      const int in_page = p.page_shift >= 0 ? key & (p.page_size - 1) : key % p.page_size;
+      const int pg = prow[s];
+      int row = p.num_pages * p.page_size;   // past the cache: TMA fills zeros
+      if (pg >= 0 && pg < p.num_pages)
+        row = pg * p.page_size + in_page;
+      else if (pg != -2)
+        atomicOr(p.status, kDevBadSeqlens);
+      prow[s] = row;
+    }
+  };
+  // K or V tile of 128-key block kb (absolute within the sequence)
+  auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb) -> bool {
     const int s = kvc % C::STAGES;
     const uint32_t ph = (kvc / C::STAGES) & 1u;
+    if (p.block_table != nullptr) page_fetch(ti, kb);
     if (!wt.wait(bar(C::kBarKVEmpty + s), ph ^ 1u, 2)) return false;
-    ptx::mbar_arrive_expect_tx(bar(C::kBarKVFull + s), C::kTileBytes);
-    load_tile(m, h, row, sbase + C::kOffKV + s * C::kTileBytes, bar(C::kBarKVFull + s));
+    const uint32_t dst = sbase + C::kOffKV + s * C::kTileBytes, b = bar(C::kBarKVFull + s);
+    ptx::mbar_arrive_expect_tx(b, C::kTileBytes);
+    if (p.block_table == nullptr) {
+      load_tile(m, ti.h, ti.ktok + 128 * kb, dst, b);
+    } else {
+      // paged: page_rows-row boxes, each from its page; rows past the
+      // sequence (or a bad page entry) point past the cache, where TMA fills
+      // zeros. page_rows is a multiple of 16, so every box starts on a
+      // 2 KB boundary of the swizzled tile.
+      page_rows(kb);
+      const int nsub = 128 / p.page_rows;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        if (s >= nsub) break;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          ptx::tma_load_2d(dst + bx * C::kBoxBytes + s * p.page_rows * 128, m, ti.h * C::D + bx * C::kBoxCols,
+                           prow[s], b);
+      }
+    }
     ++kvc;
     return true;
   };
@@ -242,18 +310,18 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     if (!ok) break;
     ++tcount;
     const int n = ti.n_kv;
-    const int krow = ti.ktok + 128 * ti.kb0;   // first key row of the tile's range
+    const int kb0 = ti.kb0;   // first key block of the tile's range
     if (C::QT == 2) {
       // consumption order of the MMA warp: K0, V0, K1, V1, ...
       for (int i = 0; ok && i < n; ++i) {
-        ok = load_kv(tk, ti.h, krow + 128 * i) && load_kv(tv, ti.h, krow + 128 * i);
+        ok = load_kv(tk, ti, kb0 + i) && load_kv(tv, ti, kb0 + i);
       }
     } else {
       // consumption order: K0, K1, V0, K2, V1, ..., V_{n-1}
-      ok = load_kv(tk, ti.h, krow);
+      ok = load_kv(tk, ti, kb0);
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n) ok = load_kv(tk, ti.h, krow + 128 * (i + 1));
-        if (ok) ok = load_kv(tv, ti.h, krow + 128 * i);
+        if (i + 1 < n) ok = load_kv(tk, ti, kb0 + i + 1);
+        if (ok) ok = load_kv(tv, ti, kb0 + i);
       }
     }
   }

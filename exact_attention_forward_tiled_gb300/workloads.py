@@ -32,6 +32,7 @@ class Workload:
     outliers: bool = False           # fp8 outlier workload
     splitkv: bool = False            # run through the split-KV forward
     backward: bool = False           # forward + backward step (an upstream gradient dO is drawn too)
+    page_size: int = 0               # > 0: K/V also laid out in a paged cache of this page size
     note: str = field(default="", compare=False)
 
 
@@ -59,6 +60,14 @@ WORKLOADS = {
                    note="bf16 backward B=4 H=16 Sq=Sk=8192 D=128 non-causal"),
     "b2": Workload("bf16_bwd_causal_B2_H16_S16384_D128", "bf16", 2, 16, 16384, 16384, 128, True, 8,
                    backward=True, note="bf16 backward causal B=2 H=16 Sq=Sk=16384 D=128"),
+    # paged K/V: Sq new queries per sequence at the end of an Sk-key context
+    # whose keys sit in shuffled 16-key pages
+    "p1": Workload("bf16_paged_prefill_B8_H16_Sq1024_Sk8192_D128_page16", "bf16", 8, 16, 1024, 8192, 128, True, 9,
+                   page_size=16, note="bf16 paged, chunked prefill: B=8 H=16, 1024 new queries against 8192 "
+                                      "cached keys (causal, bottom-right), pages of 16 keys, D=128"),
+    "p2": Workload("bf16_paged_decode_B64_H16_Sq1_Sk8192_D128_page16", "bf16", 64, 16, 1, 8192, 128, True, 10,
+                   page_size=16, note="bf16 paged decode: B=64 H=16, one query against 8192 cached keys, "
+                                      "pages of 16 keys, D=128, automatic key ranges"),
 }
 
 TORCH_DTYPE = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
@@ -131,7 +140,44 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
     out["q"], out["k"], out["v"] = q.to(dt), k.to(dt), v.to(dt)
     if w.backward:
         out["do"] = torch.randn((Tq, w.H, w.D), generator=g, device=device, dtype=torch.float32).to(dt)
+    if w.page_size:
+        out.update(paged_cache(out["k"], out["v"], [w.Sk] * w.B, w.page_size, seed))
     return out
+
+
+def paged_cache(k, v, lengths, page_size, seed, spare_pages=0):
+    """The keys and values of packed sequences (``[tokens, H, D]``, lengths
+    ``lengths``) laid out in a cache of ``page_size``-key pages in a seeded
+    random order: returns k_cache, v_cache ``[num_pages, page_size, H, D]``,
+    block_table int32 ``[B, max_pages]`` and seqlens_k int32 ``[B]``. A last
+    page's rows past its sequence are zero. Pure data movement."""
+    B = len(lengths)
+    pages_per = [(L + page_size - 1) // page_size for L in lengths]
+    num_pages = sum(pages_per) + spare_pages
+    max_pages = max(max(pages_per), 1)
+    perm = torch.randperm(num_pages, generator=_gen(seed, "cpu"))
+    H, D = k.shape[1], k.shape[2]
+    kc = torch.zeros((num_pages, page_size, H, D), dtype=k.dtype, device=k.device)
+    vc = torch.zeros_like(kc)
+    table = torch.zeros((B, max_pages), dtype=torch.int32)
+    nxt, start = 0, 0
+    for b, L in enumerate(lengths):
+        n = pages_per[b]
+        pages = perm[nxt:nxt + n]
+        nxt += n
+        table[b, :n] = pages.to(torch.int32)
+        full = L // page_size
+        dev_pages = pages.to(k.device)
+        if full:
+            kc[dev_pages[:full]] = k[start:start + full * page_size].reshape(full, page_size, H, D)
+            vc[dev_pages[:full]] = v[start:start + full * page_size].reshape(full, page_size, H, D)
+        rest = L - full * page_size
+        if rest:
+            kc[dev_pages[full], :rest] = k[start + full * page_size:start + L]
+            vc[dev_pages[full], :rest] = v[start + full * page_size:start + L]
+        start += L
+    return {"k_cache": kc, "v_cache": vc, "block_table": table.to(k.device),
+            "seqlens_k": torch.tensor(lengths, dtype=torch.int32, device=k.device)}
 
 
 def sample_rows(w: Workload, inputs, n_target=2048, seed=12345):

@@ -132,6 +132,45 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                            int num_splits, int dtype, void* stream);
 
 /*
+ * fa_fwd_paged -- fa_fwd with K and V read from a paged cache
+ * ("Flash Attention 3 principles (guijiagi)" section 5.3: PagedAttention
+ * keeps a sequence's keys in fixed-size pages named by a block table). That
+ * section gathers a sequence's pages into a contiguous buffer before
+ * attention; here the kernel's TMA loads read each page in place, so there
+ * is no gather pass and no extra copy.
+ *
+ *   q            [B*Sq, H, D] (fixed query length Sq per sequence)
+ *   k_cache, v_cache  [num_pages, page_size, H, D], same 16-bit type as q
+ *   block_table  device int32 [B, max_pages]: page of each page_size-key
+ *                block of each sequence
+ *   seqlens_k    device int32 [B]: keys of each sequence (<= max_pages *
+ *                page_size); key j of sequence b is row j % page_size of
+ *                page block_table[b][j / page_size]
+ *   o, lse       as fa_fwd with fixed length ([B*Sq, H, D], [B, H, Sq])
+ *   page_size    16, 32, 64 or a multiple of 128
+ *   num_splits   key ranges as fa_fwd_splitkv: 1 = none (workspace unused),
+ *                0 = automatic, > 1 = that many; the workspace is
+ *                fa_fwd_splitkv_workspace_size(B, H, Sq, max_pages *
+ *                page_size, D, num_splits) bytes when more than one range
+ *                is used (NULL allowed otherwise)
+ *   causal       bottom-right aligned per sequence (the Sq queries are the
+ *                last Sq positions of a sequence of seqlens_k[b] keys)
+ *
+ * Only the table entries of a sequence's first ceil(seqlens_k[b] /
+ * page_size) blocks are read. Every row of those pages must hold finite
+ * values, the rows past the sequence's length in its last page included:
+ * their scores are masked, but their V rows still meet a zero weight in the
+ * tensor-core product. An entry outside [0, num_pages) or a bad length is
+ * not dereferenced (its keys read as zeros) and is reported as
+ * FA_ERR_DEVICE_SEQLENS by fa_get_device_status; that sequence's outputs are
+ * then undefined.
+ */
+int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                 const int* seqlens_k, void* o, float* lse, int B, int H, int Sq, int D,
+                 int num_pages, int page_size, int max_pages, float scale, int causal,
+                 int num_splits, void* workspace, size_t workspace_bytes, int dtype, void* stream);
+
+/*
  * fa_fp8_prep -- FP8 preparation of the inputs ("FlashAttention-3 (lukebest
  * wiki)", technique 3: block quantisation and incoherent processing).
  *
