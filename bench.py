@@ -307,6 +307,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's number of sequences (smaller profiling cases)")
+    ap.add_argument("--page-size", type=int, default=None,
+                    help="paged workloads: override the page size; 0 runs the same shapes with contiguous K/V "
+                         "through fa_fwd")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -334,9 +337,12 @@ def main(argv=None):
     api.lib()
 
     w = workloads.WORKLOADS[args.workload]
+    from dataclasses import replace
     if args.batch is not None and not w.varlen:
-        from dataclasses import replace
         w = replace(w, B=args.batch, name=f"{w.name}_B{args.batch}")
+    if args.page_size is not None and w.page_size:
+        w = replace(w, page_size=args.page_size,
+                    name=w.name.rsplit("_page", 1)[0] + (f"_page{args.page_size}" if args.page_size else "_contiguous"))
     fp8 = w.dtype == "fp8"
     inputs = workloads.make_inputs(w, device=dev)
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
