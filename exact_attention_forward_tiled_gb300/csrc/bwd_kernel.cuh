@@ -424,14 +424,16 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
         ptx::reg_fence(xv);
         const int clo = lo - 32 * ch, chi = hi - 32 * ch;
         const bool masked = clo > 0 || chi < 32;
+        float4 nl4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           uint64_t nl2;
           if (C::DQ) {
             nl2 = ptx::f2pack(nl_row, nl_row);
           } else {
-            const float2 a = *reinterpret_cast<const float2*>(vec + 32 * ch + j);
-            nl2 = ptx::f2pack(a.x, a.y);
+            // one 16-byte broadcast load serves two column pairs
+            if ((j & 3) == 0) nl4 = *reinterpret_cast<const float4*>(vec + 32 * ch + j);
+            nl2 = (j & 3) == 0 ? ptx::f2pack(nl4.x, nl4.y) : ptx::f2pack(nl4.z, nl4.w);
           }
           float e0, e1;
           ptx::f2unpack(ptx::fma2(ptx::f2pack(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1])), c2, nl2),
@@ -465,14 +467,15 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
         ptx::tmem_wait_ld();
         ptx::reg_fence(yv);
         uint32_t pk[16];
+        float4 nd4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           uint64_t nd2;
           if (C::DQ) {
             nd2 = ptx::f2pack(nd_row, nd_row);
           } else {
-            const float2 b = *reinterpret_cast<const float2*>(vec + 64 + 32 * ch + j);
-            nd2 = ptx::f2pack(b.x, b.y);
+            if ((j & 3) == 0) nd4 = *reinterpret_cast<const float4*>(vec + 64 + 32 * ch + j);
+            nd2 = (j & 3) == 0 ? ptx::f2pack(nd4.x, nd4.y) : ptx::f2pack(nd4.z, nd4.w);
           }
           const uint64_t t = ptx::add2(ptx::f2pack(__uint_as_float(yv[j]), __uint_as_float(yv[j + 1])), nd2);
           float d0, d1;
