@@ -166,7 +166,7 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FA_ERR_ALIGNMENT;
-  const int rows = fa::cta_rows(D);
+  const int rows = fa::cta_rows16(D, Sq);
   const int64_t n_qblk = ((int64_t)Sq + rows - 1) / rows;
   const int64_t ntiles = (int64_t)B * H * n_qblk;
   if (ntiles > INT32_MAX || (int64_t)B * H * Sq > ((int64_t)1 << 40)) return FA_ERR_INVALID_ARG;
@@ -203,6 +203,7 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
   L.D = D;
   L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
   L.causal = causal != 0;
+  L.one_tile = D <= 128 && rows == 128;
   L.num_sms = dev->sms;
   L.stream = static_cast<cudaStream_t>(stream);
   return FA_OK;
@@ -212,8 +213,8 @@ int launch16(fa::FwdLaunch& L, DevInfo* dev) {
   L.p.sched = dev->take_slot();
   cudaError_t e;
   switch (L.D) {
-    case 64: e = fa::launch_fwd_d64(L); break;
-    case 128: e = fa::launch_fwd_d128(L); break;
+    case 64: e = L.one_tile ? fa::launch_fwd_d64_q1(L) : fa::launch_fwd_d64(L); break;
+    case 128: e = L.one_tile ? fa::launch_fwd_d128_q1(L) : fa::launch_fwd_d128(L); break;
     default: e = fa::launch_fwd_d256(L); break;
   }
   if (e != cudaSuccess) {
@@ -229,7 +230,7 @@ int launch16(fa::FwdLaunch& L, DevInfo* dev) {
 void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms, int* n_split,
                     int* split_blocks) {
   const int64_t nblocks = ((int64_t)Sk + 127) / 128;
-  const int rows = fa::cta_rows(D);
+  const int rows = fa::cta_rows16(D, Sq);
   const int64_t tiles = (int64_t)B * H * (((int64_t)Sq + rows - 1) / rows);
   int64_t n = requested;
   if (n <= 0) n = tiles > 0 ? (2 * (int64_t)sms + tiles - 1) / tiles : 1;
@@ -347,6 +348,8 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
   L.p.num_pages = num_pages;
   L.p.page_rows = (int)box_rows;
   L.p.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
+  L.p.n_kblk_tag = Sk / 128 + 2;
+  if ((int64_t)B * L.p.n_kblk_tag > INT32_MAX) return FA_ERR_INVALID_ARG;
   int n = 1, per = 1;
   resolve_splits(B, H, Sq, Sk, D, num_splits, dev->sms, &n, &per);
   if (num_splits == 1) n = 1;

@@ -57,6 +57,7 @@ struct FwdParams {
   const int* seqlens_k;
   int max_pages, page_size, num_pages, page_rows;
   int page_shift;   // log2(page_size) for a power of two, else -1
+  int n_kblk_tag;   // max_pages * page_size / 128 + 1: tags a (sequence, key block) pair
 };
 
 // Element kinds of the attention inputs.
@@ -69,15 +70,22 @@ struct FwdLaunch {
   int D;
   int kind;  // Kind
   bool causal;
+  bool one_tile;  // D <= 128 with one query tile per work tile (short queries)
   int num_sms;
   cudaStream_t stream;
 };
 
 // Rows of Q per CTA for head dimension D (2 x 128 for D <= 128, 128 for 256).
 constexpr int cta_rows(int D) { return D <= 128 ? 256 : 128; }
+// 16-bit inputs: query sequences of at most 128 rows (decode, short chunks)
+// take the one-query-tile configuration at every D, so no work tile carries
+// a second, empty query tile through the MMAs and the softmax.
+constexpr int cta_rows16(int D, int Sq) { return (D <= 128 && Sq > 128) ? 256 : 128; }
 
 cudaError_t launch_fwd_d64(const FwdLaunch& L);
 cudaError_t launch_fwd_d128(const FwdLaunch& L);
+cudaError_t launch_fwd_d64_q1(const FwdLaunch& L);
+cudaError_t launch_fwd_d128_q1(const FwdLaunch& L);
 cudaError_t launch_fwd_d256(const FwdLaunch& L);
 cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                                  int n_split, int B, int H, int Sq, int D, int out_fp16, cudaStream_t stream);

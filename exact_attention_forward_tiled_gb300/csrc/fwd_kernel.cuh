@@ -224,42 +224,50 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     for (int bx = 0; bx < C::kBoxes; ++bx)
       ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
   };
-  // paged K/V: rows of the (up to 8) page_rows-row boxes of one 128-key
-  // block, looked up once per block (K and V share them). page_fetch issues
-  // the block-table reads before the caller waits for a free slot, and
-  // page_rows computes the rows after it, so the table's load latency hides
-  // behind the wait. Page sizes that are powers of two divide by shifting.
-  int rows_b = -1, rows_kb = -1, fetched_b = -1, fetched_kb = -1;
-  int prow[8];
+  // paged K/V: rows of the (up to 8) page_rows-row boxes of a 128-key block,
+  // looked up once per block. The one-query-tile configuration caches two
+  // blocks (entries A and B), since its order K0, K1, V0, K2, V1, ...
+  // alternates between two; the two-tile one needs entry A only. page_fetch issues a block's table reads before the caller waits
+  // for a free slot, page_rows turns them into rows after the wait, so the
+  // table's load latency hides behind the wait. Page sizes that are powers
+  // of two divide by shifting.
+  int tag_a = -1, tag_b = -1;       // pack_tag of the cached blocks
+  int rows_a[8], rows_b[8];
+  bool raw_a = false, raw_b = false, next_a = true, use_a = true;
+  auto pack_tag = [&](const TileInfo& ti, int kb) { return ti.b * p.n_kblk_tag + kb; };
   auto page_fetch = [&](const TileInfo& ti, int kb) {
-    if ((ti.b == rows_b && kb == rows_kb) || (ti.b == fetched_b && kb == fetched_kb)) return;
-    fetched_b = ti.b;
-    fetched_kb = kb;
+    const int tag = pack_tag(ti, kb);
+    if (tag == tag_a) { use_a = true; return; }
+    if (C::QT == 1 && tag == tag_b) { use_a = false; return; }
+    // two query tiles load K_i, V_i in pairs: one entry is enough
+    use_a = C::QT == 2 ? true : next_a;
+    next_a = !next_a;
     const int nsub = 128 / p.page_rows;
     const int* tab = p.block_table + (int64_t)ti.b * p.max_pages;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int key = 128 * kb + s * p.page_rows;
       const int pi = p.page_shift >= 0 ? key >> p.page_shift : key / p.page_size;
-      prow[s] = (s < nsub && key < ti.Lk) ? __ldg(tab + pi) : -2;   // -2: a box past the sequence
+      const int pg = (s < nsub && key < ti.Lk) ? __ldg(tab + pi) : -2;   // -2: a box past the sequence
+      if (use_a) rows_a[s] = pg; else rows_b[s] = pg;
     }
+    if (use_a) { tag_a = tag; raw_a = true; } else { tag_b = tag; raw_b = true; }
   };
   auto page_rows = [&](int kb) {
-    if (fetched_b == rows_b && fetched_kb == rows_kb) return;
-    rows_b = fetched_b;
-    rows_kb = fetched_kb;
+    if (use_a ? !raw_a : !raw_b) return;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int key = 128 * kb + s * p.page_rows;
       const int in_page = p.page_shift >= 0 ? key & (p.page_size - 1) : key % p.page_size;
-      const int pg = prow[s];
+      const int pg = use_a ? rows_a[s] : rows_b[s];
       int row = p.num_pages * p.page_size;   // past the cache: TMA fills zeros
       if (pg >= 0 && pg < p.num_pages)
         row = pg * p.page_size + in_page;
       else if (pg != -2)
         atomicOr(p.status, kDevBadSeqlens);
-      prow[s] = row;
+      if (use_a) rows_a[s] = row; else rows_b[s] = row;
     }
+    if (use_a) raw_a = false; else raw_b = false;
   };
   // K or V tile of 128-key block kb (absolute within the sequence)
   auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb) -> bool {
@@ -281,10 +289,11 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         if (s >= nsub) break;
+        const int row = use_a ? rows_a[s] : rows_b[s];
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
           ptx::tma_load_2d(dst + bx * C::kBoxBytes + s * p.page_rows * 128, m, ti.h * C::D + bx * C::kBoxCols,
-                           prow[s], b);
+                           row, b);
       }
     }
     ++kvc;
