@@ -96,7 +96,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 128-byte swizzle (the layout the tcgen05 descriptors expect), zero fill
 // outside the matrix.
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t cols,
-             uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+             uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return FA_ERR_CUDA;
   cuuint64_t dims[2] = {cols, rows < 1 ? 1 : rows};
@@ -104,7 +105,7 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
@@ -431,7 +432,18 @@ int prep_impl(const void* q, const void* k, const void* v, int in_dtype, void* q
     add(k, k8, k_scale, sigma, Sk, cu_k, cbk, total_k);
     add(v, v8, v_scale, nullptr, Sk, cu_k, cbk, total_k);
   }
-  cudaError_t e = fa::launch_fp8_prep(t, n, D, static_cast<cudaStream_t>(stream));
+  // one [rows, H * D] map per tensor; a box is one 128-row block of one head,
+  // unswizzled (the preparation reads it row by row from shared memory)
+  CUtensorMap maps[3];
+  const CUtensorMapDataType dt = in_dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  for (int i = 0; i < n; ++i) {
+    const uint64_t rows = t[i].cu_seqlens != nullptr ? (uint64_t)t[i].total : (uint64_t)t[i].B * t[i].S;
+    if ((st = make_map(&maps[i], t[i].x, dt, 2, (uint64_t)H * D, rows, (uint32_t)D, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != FA_OK)
+      return st;
+  }
+  cudaError_t e = fa::launch_fp8_prep(t, maps, n, D, dev->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;

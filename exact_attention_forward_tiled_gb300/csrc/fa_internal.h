@@ -146,6 +146,8 @@ struct PrepParams {
   int* status;            // device status word (bad cu_seqlens entries)
 };
 cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, cudaStream_t stream);
-cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cudaStream_t stream);
+// maps: [rows, H * D] tensor maps of the inputs with one 128-row x D box
+cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* maps, int n_tensors, int D, int num_sms,
+                            cudaStream_t stream);
 
 }  // namespace fa

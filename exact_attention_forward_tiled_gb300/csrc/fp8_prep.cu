@@ -5,11 +5,12 @@
 // 128-row block of each (sequence, head): scale = amax / 448 (1 for an
 // all-zero block), code = e4m3(x / scale), round to nearest even, saturating.
 //
-// One CTA owns one 128 x D block of one tensor and keeps it in registers:
-// the Walsh-Hadamard transform runs there (butterflies over the bits of d
-// inside a lane, then across lanes with shuffles), the block amax is reduced
-// through shared memory, and only then are the codes written, so every
-// element is read from HBM once and written once.
+// Persistent CTAs walk the 128 x D blocks (one head of one tensor each); a
+// TMA copy brings the next block into shared memory while the current one is
+// rotated in registers (butterflies over the bits of d inside a lane, then
+// across lanes with shuffles), its amax is reduced through shared memory and
+// its codes are written, so every element is read from HBM once and written
+// once, with reads in flight throughout.
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -24,47 +25,47 @@ struct PrepBatch {
   int n;
 };
 
-// Eight consecutive 16-bit elements (16 bytes) -> fp32.
-__device__ __forceinline__ void load8(const PrepParams& P, int64_t off, float (&x)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(P.x) + off));
+// Eight consecutive 16-bit elements (16 bytes, read from shared memory) -> fp32.
+__device__ __forceinline__ void cvt8(uint4 u, bool bf16, float (&x)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint16_t lo = w[k] & 0xffffu, hi = w[k] >> 16;
-    x[2 * k] = P.bf16 ? __uint_as_float((uint32_t)lo << 16) : __half2float(__ushort_as_half(lo));
-    x[2 * k + 1] = P.bf16 ? __uint_as_float((uint32_t)hi << 16) : __half2float(__ushort_as_half(hi));
+    x[2 * k] = bf16 ? __uint_as_float((uint32_t)lo << 16) : __half2float(__ushort_as_half(lo));
+    x[2 * k + 1] = bf16 ? __uint_as_float((uint32_t)hi << 16) : __half2float(__ushort_as_half(hi));
   }
 }
 
-// CTA = one 128-row block of one (sequence, head) of one tensor. A row is
-// spread over LPR = D/8 lanes holding 8 consecutive elements each (16-byte
-// loads, 8-byte stores), so one warp instruction covers 32/LPR rows.
-// Consecutive CTAs take consecutive heads of the same rows, so the CTAs in
-// flight read whole [token, H*D] rows of HBM.
-template <int D>
-__global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) fp8_prep_kernel(const PrepBatch pb) {
-  constexpr int NW = D == 256 ? 32 : 16;  // warps per CTA (4 loads in flight per lane)
-  constexpr int LPR = D / 8;               // lanes per row
-  constexpr int RPI = 32 / LPR;            // rows per warp instruction
-  constexpr int RPW = 128 / NW;            // rows per warp
-  constexpr int ITER = RPW / RPI;
-  constexpr int LOG_D = D == 64 ? 6 : (D == 128 ? 7 : 8);
-  __shared__ float red[NW];
+struct PrepMaps {
+  CUtensorMap m[3];
+};
 
-  int bid = blockIdx.x, ti = 0;
+// shared-memory block buffers per CTA (NB - 1 blocks fetched ahead)
+constexpr int kPrepBuffers = 2;
+
+// Where block `bid` (counted over all tensors of the batch) lives: tensor,
+// head, first token, valid rows, scale index; false if the block starts past
+// its sequence (varlen) or its sequence breaks its bounds (reported).
+struct PrepBlock {
+  int ti, h, blk, L;
+  int64_t start, sidx;
+};
+
+__device__ __forceinline__ bool prep_block(const PrepBatch& pb, int bid, PrepBlock& o) {
+  int ti = 0;
   while (ti < pb.n - 1 && bid >= pb.count[ti]) {
     bid -= pb.count[ti];
     ++ti;
   }
   const PrepParams& P = pb.t[ti];
-  const int h = bid % P.H;
+  o.ti = ti;
+  o.h = bid % P.H;
   const int rest = bid / P.H;
   const int b = rest % P.B;
-  const int blk = rest / P.B;
-  // the block's rows: tokens start + [blk * 128, min(blk * 128 + 128, L))
-  int64_t start = (int64_t)b * P.S;
-  int L = P.S;
-  int64_t sidx = ((int64_t)b * P.H + h) * P.nblk + blk;   // where its scale goes
+  o.blk = rest / P.B;
+  o.start = (int64_t)b * P.S;
+  o.L = P.S;
+  o.sidx = ((int64_t)b * P.H + o.h) * P.nblk + o.blk;
   if (P.cu_seqlens != nullptr) {
     const int s0 = __ldg(P.cu_seqlens + b), s1 = __ldg(P.cu_seqlens + b + 1);
     const int c0 = __ldg(P.cu_blocks + b), c1 = __ldg(P.cu_blocks + b + 1), cn = __ldg(P.cu_blocks + P.B);
@@ -73,90 +74,172 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2) f
     // [n_blocks, H] scale arrays: skipped and reported
     if (s0 < 0 || s1 < s0 || s1 > P.total || s1 - s0 > P.S || c0 < 0 || c1 - c0 != (s1 - s0 + 127) / 128 ||
         c1 > cn || cn > P.total / 128 + P.B) {
-      if (threadIdx.x == 0 && blk == 0 && h == 0) atomicOr(P.status, kDevBadSeqlens);
-      return;
+      if (threadIdx.x == 0 && o.blk == 0 && o.h == 0) atomicOr(P.status, kDevBadSeqlens);
+      return false;
     }
-    start = s0;
-    L = s1 - s0;
-    if (blk * 128 >= L) return;   // the whole CTA leaves together
-    sidx = (int64_t)(c0 + blk) * P.H + h;
+    o.start = s0;
+    o.L = s1 - s0;
+    if (o.blk * 128 >= o.L) return false;
+    o.sidx = (int64_t)(c0 + o.blk) * P.H + o.h;
   }
+  return true;
+}
+
+// Persistent CTAs, each walking blocks bid = blockIdx.x, + gridDim.x, ...
+// A block is 128 rows x D of one head of one tensor. Thread 0 fetches the
+// next block with one TMA copy into the other half of a shared-memory double
+// buffer while the CTA works on the current one, so HBM reads stay in flight
+// while the CTA rotates, reduces and stores.
+//
+// The work on a block: a row is spread over LPR = D/8 lanes holding 8
+// consecutive elements each; the Walsh-Hadamard transform runs in registers
+// (butterflies over the bits of d inside a lane, then across lanes with
+// shuffles), the block amax is reduced through shared memory, and the codes
+// are written with 8-byte stores.
+template <int D>
+__global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2)
+    fp8_prep_kernel(const __grid_constant__ PrepMaps maps, const PrepBatch pb, int total_blocks) {
+  constexpr int NW = D == 256 ? 32 : 16;  // warps per CTA
+  constexpr int LPR = D / 8;               // lanes per row
+  constexpr int RPI = 32 / LPR;            // rows per warp instruction
+  constexpr int RPW = 128 / NW;            // rows per warp
+  constexpr int ITER = RPW / RPI;
+  constexpr int LOG_D = D == 64 ? 6 : (D == 128 ? 7 : 8);
+  constexpr uint32_t kBlockBytes = 128u * D * 2u;
+  constexpr int NB = kPrepBuffers;
+  extern __shared__ __align__(128) uint8_t prep_smem[];
+  __shared__ float red[NW];
+  __shared__ __align__(8) uint64_t full_bar[NB];
+  __shared__ int gave_up;
+  const uint32_t buf0 = ptx::smem_u32(prep_smem);
+  const uint32_t bar0 = ptx::smem_u32(&full_bar[0]);
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPR;              // row of the instruction this lane serves
   const int d0 = (lane % LPR) * 8;         // first element of the lane
 
-  float sg[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) sg[j] = P.sigma ? (float)P.sigma[d0 + j] : 1.f;
-  // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
-  const float norm = P.sigma ? rsqrtf((float)D) : 1.f;
-
-  float x[ITER][8];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < ITER; ++i) {
-    const int row = blk * 128 + warp * RPW + i * RPI + sub;
-    if (row < L) {
-      load8(P, ((start + row) * P.H + h) * D + d0, x[i]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
-    }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NB; ++i) ptx::mbar_init(bar0 + 8u * i, 1);
+    ptx::fence_mbar_init();
+    gave_up = 0;
   }
-#pragma unroll
-  for (int i = 0; i < ITER; ++i) {
-    if (P.sigma) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[i][j] *= sg[j];
-      // Walsh-Hadamard butterflies over the three bits of d inside the lane
-#pragma unroll
-      for (int bit = 0; bit < 3; ++bit) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j & (1 << bit)) continue;
-          const float a = x[i][j], c = x[i][j | (1 << bit)];
-          x[i][j] = a + c;
-          x[i][j | (1 << bit)] = a - c;
-        }
-      }
-      // ... and over the bits of d that select the lane (within the row's
-      // lanes): lower partner a + b, upper partner a - b = other - mine, one
-      // FFMA each with the sign of the lane's half
-#pragma unroll
-      for (int bit = 3; bit < LOG_D; ++bit) {
-        const int m = 1 << (bit - 3);
-        const float sgn = (lane & m) ? -1.f : 1.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[i][j], m);
-          x[i][j] = fmaf(x[i][j], sgn, other);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
-  }
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  if (lane == 0) red[warp] = amax;
   __syncthreads();
-  amax = red[0];
+
+  // thread 0: fetch block `bid` into buffer `s` (nothing if it is skipped)
+  auto fetch = [&](int bid, int s) {
+    PrepBlock pbk;
+    if (bid < total_blocks && prep_block(pb, bid, pbk)) {
+      ptx::mbar_arrive_expect_tx(bar0 + 8u * s, kBlockBytes);
+      ptx::tma_load_2d(buf0 + s * kBlockBytes, &maps.m[pbk.ti], pbk.h * D, (int)(pbk.start + pbk.blk * 128),
+                       bar0 + 8u * s);
+    }
+  };
+  // NB - 1 blocks ahead
+  if (threadIdx.x == 0)
+    for (int i = 0; i < NB - 1; ++i) fetch(blockIdx.x + i * gridDim.x, i);
+  uint32_t phase_bits = 0u;   // bit i: parity of buffer i's next completion
+
+  int s = 0;
+  for (int bid = blockIdx.x; bid < total_blocks; bid += gridDim.x, s = (s + 1) % NB) {
+    PrepBlock pbk;
+    const bool live = prep_block(pb, bid, pbk);
+    // block bid + (NB - 1) * gridDim.x goes into the buffer the previous
+    // iteration used, free since the __syncthreads that ended it
+    if (threadIdx.x == 0) fetch(bid + (NB - 1) * gridDim.x, (s + NB - 1) % NB);
+    if (!live) continue;
+    const PrepParams& P = pb.t[pbk.ti];
+    // bounded wait for this block's copy: thread 0 waits, the CTA learns the
+    // outcome at the barrier (the barrier also publishes the copied data)
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar0 + 8u * s, (phase_bits >> s) & 1u)) {
+        if (ptx::globaltimer_ns() - t0 > 2000000000ull) {
+          atomicOr(P.status, kDevTimeout | 0x40);
+          gave_up = 1;
+          break;
+        }
+      }
+    }
+    phase_bits ^= 1u << s;
+    __syncthreads();
+    if (gave_up) return;
+    const uint8_t* blkmem = prep_smem + s * kBlockBytes;
+
+    float sg[8];
 #pragma unroll
-  for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
-  amax *= norm;   // amax of the rotated, normalised values
-  const float scale = amax > 0.f ? amax / 448.f : 1.f;
-  const float inv = norm / scale;
-  if (threadIdx.x == 0) P.scale[sidx] = scale;
+    for (int j = 0; j < 8; ++j) sg[j] = P.sigma ? (float)P.sigma[d0 + j] : 1.f;
+    // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
+    const float norm = P.sigma ? rsqrtf((float)D) : 1.f;
+
+    float x[ITER][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < ITER; ++i) {
+      const int row = warp * RPW + i * RPI + sub;   // within the block
+      if (pbk.blk * 128 + row < pbk.L) {
+        cvt8(*reinterpret_cast<const uint4*>(blkmem + (row * D + d0) * 2), P.bf16, x[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < ITER; ++i) {
+      if (P.sigma) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] *= sg[j];
+        // Walsh-Hadamard butterflies over the three bits of d inside the lane
+#pragma unroll
+        for (int bit = 0; bit < 3; ++bit) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j & (1 << bit)) continue;
+            const float a = x[i][j], c = x[i][j | (1 << bit)];
+            x[i][j] = a + c;
+            x[i][j | (1 << bit)] = a - c;
+          }
+        }
+        // ... and over the bits of d that select the lane (within the row's
+        // lanes): lower partner a + b, upper partner a - b = other - mine, one
+        // FFMA each with the sign of the lane's half
+#pragma unroll
+        for (int bit = 3; bit < LOG_D; ++bit) {
+          const int m = 1 << (bit - 3);
+          const float sgn = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[i][j], m);
+            x[i][j] = fmaf(x[i][j], sgn, other);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
+    amax *= norm;   // amax of the rotated, normalised values
+    const float scale = amax > 0.f ? amax / 448.f : 1.f;
+    const float inv = norm / scale;
+    if (threadIdx.x == 0) P.scale[pbk.sidx] = scale;
 
 #pragma unroll
-  for (int i = 0; i < ITER; ++i) {
-    const int row = blk * 128 + warp * RPW + i * RPI + sub;
-    if (row >= L) continue;
-    uint32_t w[4];
+    for (int i = 0; i < ITER; ++i) {
+      const int row = pbk.blk * 128 + warp * RPW + i * RPI + sub;
+      if (row >= pbk.L) continue;
+      uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
-    *reinterpret_cast<uint2*>(P.x8 + ((start + row) * P.H + h) * D + d0) =
-        make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+      for (int j = 0; j < 4; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
+      *reinterpret_cast<uint2*>(P.x8 + ((pbk.start + row) * P.H + pbk.h) * D + d0) =
+          make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    }
+    // red[] and this buffer are reused by the next iterations
+    __syncthreads();
   }
 }
 
@@ -178,23 +261,44 @@ cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_fp8_prep(const PrepParams* tensors, int n_tensors, int D, cudaStream_t stream) {
+cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* maps, int n_tensors, int D, int num_sms,
+                            cudaStream_t stream) {
   PrepBatch pb{};
+  PrepMaps pm{};
   long total = 0;
   pb.n = n_tensors;
   for (int i = 0; i < n_tensors; ++i) {
     pb.t[i] = tensors[i];
+    pm.m[i] = maps[i];
     pb.count[i] = tensors[i].B * tensors[i].H * tensors[i].nblk;
     total += pb.count[i];
   }
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffL) return cudaErrorInvalidValue;
+  // resident CTAs: two per SM for D <= 128 (64 registers x 512 threads,
+  // kPrepBuffers 128-row blocks of shared memory each), one for D = 256
+  // (1024 threads)
+  const long per_sm = D == 256 ? 1L : 2L;
+  const int grid = (int)(total < per_sm * num_sms ? total : per_sm * num_sms);
+  const size_t smem = (size_t)kPrepBuffers * 128u * (size_t)D * 2u;
+  cudaError_t e;
   switch (D) {
-    case 64: fp8_prep_kernel<64><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
-    case 128: fp8_prep_kernel<128><<<(unsigned)total, 32 * 16, 0, stream>>>(pb); break;
-    case 256: fp8_prep_kernel<256><<<(unsigned)total, 32 * 32, 0, stream>>>(pb); break;
-    default: return cudaErrorInvalidValue;
+    case 64:
+      e = cudaFuncSetAttribute(fp8_prep_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) fp8_prep_kernel<64><<<grid, 32 * 16, smem, stream>>>(pm, pb, (int)total);
+      break;
+    case 128:
+      e = cudaFuncSetAttribute(fp8_prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) fp8_prep_kernel<128><<<grid, 32 * 16, smem, stream>>>(pm, pb, (int)total);
+      break;
+    case 256:
+      e = cudaFuncSetAttribute(fp8_prep_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) fp8_prep_kernel<256><<<grid, 32 * 32, smem, stream>>>(pm, pb, (int)total);
+      break;
+    default:
+      return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
