@@ -227,10 +227,11 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   // paged K/V: rows of the (up to 8) page_rows-row boxes of a 128-key block,
   // looked up once per block. The one-query-tile configuration caches two
   // blocks (entries A and B), since its order K0, K1, V0, K2, V1, ...
-  // alternates between two; the two-tile one needs entry A only. page_fetch issues a block's table reads before the caller waits
-  // for a free slot, page_rows turns them into rows after the wait, so the
-  // table's load latency hides behind the wait. Page sizes that are powers
-  // of two divide by shifting.
+  // alternates between two; the two-tile one needs entry A only. page_fetch
+  // issues a block's table reads before the caller waits for a free slot,
+  // page_rows turns them into rows after the wait, so the table's load
+  // latency hides behind the wait. Page sizes that are powers of two divide
+  // by shifting.
   int tag_a = -1, tag_b = -1;       // pack_tag of the cached blocks
   int rows_a[8], rows_b[8];
   bool raw_a = false, raw_b = false, next_a = true, use_a = true;
