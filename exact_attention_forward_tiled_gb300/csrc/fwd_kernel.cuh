@@ -211,29 +211,43 @@ __device__ __forceinline__ int fetch_tile(const FwdParams& p, int j) {
 }
 
 // ------------------------------------------------------------------ load warp
+// The whole warp runs this role. Lane 0 does the waits, the tile ring and the
+// contiguous TMA loads; for paged K/V every lane s < 128 / page_rows looks up,
+// and loads, box s of a tile itself, so a tile's block-table reads and copies
+// are issued in parallel rather than one after another.
 template <class C, bool CAUSAL>
 __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                           const FwdParams& p, uint32_t sbase, const Waiter& wt, const TileRing& ring) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
+  const int lane = threadIdx.x & 31;
+  const bool lead = lane == 0;
   uint32_t kvc = 0, tcount = 0;
   bool ok = true;
+  // lane 0 waits; every lane learns the outcome
+  auto wait0 = [&](uint32_t b, uint32_t parity, int where) -> bool {
+    bool r = true;
+    if (lead) r = wt.wait(b, parity, where);
+    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+  };
 
   auto load_tile = [&](const CUtensorMap* m, int h, int row, uint32_t dst, uint32_t b) {
 #pragma unroll
     for (int bx = 0; bx < C::kBoxes; ++bx)
       ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
   };
-  // paged K/V: rows of the (up to 8) page_rows-row boxes of a 128-key block,
-  // looked up once per block. The one-query-tile configuration caches two
+  // paged K/V: lane s's row for box s of a 128-key block, looked up once per
+  // block (K and V share it). The one-query-tile configuration caches two
   // blocks (entries A and B), since its order K0, K1, V0, K2, V1, ...
   // alternates between two; the two-tile one needs entry A only. page_fetch
-  // issues a block's table reads before the caller waits for a free slot,
-  // page_rows turns them into rows after the wait, so the table's load
-  // latency hides behind the wait. Page sizes that are powers of two divide
-  // by shifting.
+  // issues the lane's block-table read before lane 0 waits for a free slot,
+  // page_rows turns it into a row after the wait, so the read's latency hides
+  // behind the wait. Page sizes that are powers of two divide by shifting.
+  const bool paged = p.block_table != nullptr;
+  const int nsub = paged ? 128 / p.page_rows : 0;
+  const bool my_box = lane < nsub;
   int tag_a = -1, tag_b = -1;       // pack_tag of the cached blocks
-  int rows_a[8], rows_b[8];
+  int row_a = 0, row_b = 0;
   bool raw_a = false, raw_b = false, next_a = true, use_a = true;
   auto pack_tag = [&](const TileInfo& ti, int kb) { return ti.b * p.n_kblk_tag + kb; };
   auto page_fetch = [&](const TileInfo& ti, int kb) {
@@ -243,57 +257,52 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     // two query tiles load K_i, V_i in pairs: one entry is enough
     use_a = C::QT == 2 ? true : next_a;
     next_a = !next_a;
-    const int nsub = 128 / p.page_rows;
-    const int* tab = p.block_table + (int64_t)ti.b * p.max_pages;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int key = 128 * kb + s * p.page_rows;
+    const int key = 128 * kb + lane * p.page_rows;
+    int pg = -2;   // -2: a box past the sequence
+    if (my_box && key < ti.Lk) {
       const int pi = p.page_shift >= 0 ? key >> p.page_shift : key / p.page_size;
-      const int pg = (s < nsub && key < ti.Lk) ? __ldg(tab + pi) : -2;   // -2: a box past the sequence
-      if (use_a) rows_a[s] = pg; else rows_b[s] = pg;
+      pg = __ldg(p.block_table + (int64_t)ti.b * p.max_pages + pi);
     }
-    if (use_a) { tag_a = tag; raw_a = true; } else { tag_b = tag; raw_b = true; }
+    if (use_a) { row_a = pg; tag_a = tag; raw_a = true; } else { row_b = pg; tag_b = tag; raw_b = true; }
   };
-  auto page_rows = [&](int kb) {
-    if (use_a ? !raw_a : !raw_b) return;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int key = 128 * kb + s * p.page_rows;
+  auto page_rows = [&](int kb) -> int {
+    int& row = use_a ? row_a : row_b;
+    bool& raw = use_a ? raw_a : raw_b;
+    if (raw) {
+      const int key = 128 * kb + lane * p.page_rows;
       const int in_page = p.page_shift >= 0 ? key & (p.page_size - 1) : key % p.page_size;
-      const int pg = use_a ? rows_a[s] : rows_b[s];
-      int row = p.num_pages * p.page_size;   // past the cache: TMA fills zeros
+      const int pg = row;
+      row = p.num_pages * p.page_size;   // past the cache: TMA fills zeros
       if (pg >= 0 && pg < p.num_pages)
         row = pg * p.page_size + in_page;
       else if (pg != -2)
         atomicOr(p.status, kDevBadSeqlens);
-      if (use_a) rows_a[s] = row; else rows_b[s] = row;
+      raw = false;
     }
-    if (use_a) raw_a = false; else raw_b = false;
+    return row;
   };
   // K or V tile of 128-key block kb (absolute within the sequence)
   auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb) -> bool {
     const int s = kvc % C::STAGES;
     const uint32_t ph = (kvc / C::STAGES) & 1u;
-    if (p.block_table != nullptr) page_fetch(ti, kb);
-    if (!wt.wait(bar(C::kBarKVEmpty + s), ph ^ 1u, 2)) return false;
+    if (paged) page_fetch(ti, kb);
+    if (!wait0(bar(C::kBarKVEmpty + s), ph ^ 1u, 2)) return false;
     const uint32_t dst = sbase + C::kOffKV + s * C::kTileBytes, b = bar(C::kBarKVFull + s);
-    ptx::mbar_arrive_expect_tx(b, C::kTileBytes);
-    if (p.block_table == nullptr) {
-      load_tile(m, ti.h, ti.ktok + 128 * kb, dst, b);
+    if (lead) ptx::mbar_arrive_expect_tx(b, C::kTileBytes);
+    if (!paged) {
+      if (lead) load_tile(m, ti.h, ti.ktok + 128 * kb, dst, b);
     } else {
       // paged: page_rows-row boxes, each from its page; rows past the
       // sequence (or a bad page entry) point past the cache, where TMA fills
       // zeros. page_rows is a multiple of 16, so every box starts on a
-      // 2 KB boundary of the swizzled tile.
-      page_rows(kb);
-      const int nsub = 128 / p.page_rows;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        if (s >= nsub) break;
-        const int row = use_a ? rows_a[s] : rows_b[s];
+      // 2 KB boundary of the swizzled tile. The expected byte count is set
+      // before any lane's copy is issued.
+      const int row = page_rows(kb);
+      __syncwarp();
+      if (my_box) {
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
-          ptx::tma_load_2d(dst + bx * C::kBoxBytes + s * p.page_rows * 128, m, ti.h * C::D + bx * C::kBoxCols,
+          ptx::tma_load_2d(dst + bx * C::kBoxBytes + lane * p.page_rows * 128, m, ti.h * C::D + bx * C::kBoxCols,
                            row, b);
       }
     }
@@ -303,19 +312,25 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
 
   for (int j = 0; ok; ++j) {
     const int rs = j % C::kTileRing;
-    if (!wt.wait(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 9)) break;
-    const int w = fetch_tile<C::kTileRing>(p, j);
-    ring.slots[rs] = w;
-    ptx::mbar_arrive(ring.full(rs));
+    if (!wait0(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 9)) break;
+    int w = 0;
+    if (lead) {
+      w = fetch_tile<C::kTileRing>(p, j);
+      ring.slots[rs] = w;
+      ptx::mbar_arrive(ring.full(rs));
+    }
+    w = __shfl_sync(0xffffffffu, w, 0);
     if (w < 0) break;
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
 #pragma unroll
     for (int t = 0; t < C::QT; ++t) {
-      if (!wt.wait(bar(C::kBarQEmpty + t), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
-      ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
-      load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
-                bar(C::kBarQFull + t));
+      if (!wait0(bar(C::kBarQEmpty + t), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
+      if (lead) {
+        ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+        load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
+                  bar(C::kBarQFull + t));
+      }
     }
     if (!ok) break;
     ++tcount;
@@ -335,7 +350,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
       }
     }
   }
-  if (*wt.abort_flag) {
+  if (lead && *wt.abort_flag) {
     // let the copies still in flight land before the CTA's memory goes away
     const uint32_t first = kvc > (uint32_t)C::STAGES ? kvc - C::STAGES : 0u;
     for (uint32_t c = first; c < kvc; ++c)
@@ -787,7 +802,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kRebalance) ptx::setmaxnreg_dec<C::kRegsLow>();
     if (warp == C::kLoadWarp) {
-      if (lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
+      load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
     } else if (warp == C::kMmaWarp) {
       if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt, ring);
     }
