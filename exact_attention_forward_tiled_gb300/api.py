@@ -60,8 +60,8 @@ def lib():
         L.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, i, i, i, i, i,
                                         f, i, vp]
         L.fa_fwd_paged.restype = i
-        L.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t,
-                                   i, vp]
+        L.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, i, i, vp,
+                                   ctypes.c_size_t, i, vp]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd_workspace_size.argtypes = [i, i]
         L.fa_bwd.restype = i
@@ -410,39 +410,42 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, scale=None, cu_se
 
 
 def fa_fwd_paged(q, k_cache, v_cache, block_table, seqlens_k, o, lse, B, H, Sq, D, num_pages, page_size, max_pages,
-                 scale, causal, num_splits=1, workspace=None, workspace_bytes=0, dtype=None, stream=None,
-                 check=True) -> int:
+                 scale, causal, num_splits=1, workspace=None, workspace_bytes=0, cu_seqlens_q=None, total_q=0,
+                 dtype=None, stream=None, check=True) -> int:
     """Raw entry point: attention over K/V held in a paged cache."""
     if dtype is None:
         dtype = _DTYPE[q.dtype]
     st = lib().fa_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seqlens_k), _ptr(o),
                             _ptr(lse), int(B), int(H), int(Sq), int(D), int(num_pages), int(page_size),
-                            int(max_pages), float(scale), int(bool(causal)), int(num_splits), _ptr(workspace),
-                            int(workspace_bytes), int(dtype), _stream(stream))
+                            int(max_pages), float(scale), int(bool(causal)), _ptr(cu_seqlens_q), int(total_q),
+                            int(num_splits), _ptr(workspace), int(workspace_bytes), int(dtype), _stream(stream))
     if check and st != FA_OK:
         raise FAError(st, "fa_fwd_paged")
     return st
 
 
 def attention_forward_paged(q, k_cache, v_cache, block_table, seqlens_k, *, causal=False, scale=None, num_splits=1,
-                            out=None, lse=None, stream=None):
+                            cu_seqlens_q=None, max_seqlen_q=None, out=None, lse=None, stream=None):
     """Allocate O, LSE (and the split workspace) and call ``fa_fwd_paged``.
-    q ``[B*Sq, H, D]``; caches ``[num_pages, page_size, H, D]``; block_table
-    int32 ``[B, max_pages]``; seqlens_k int32 ``[B]``. Returns (O, LSE
-    ``[B, H, Sq]``)."""
+    q ``[B*Sq, H, D]`` (or packed ``[total_q, H, D]`` with ``cu_seqlens_q``
+    and ``max_seqlen_q``); caches ``[num_pages, page_size, H, D]``;
+    block_table int32 ``[B, max_pages]``; seqlens_k int32 ``[B]``. Returns
+    (O, LSE ``[B, H, Sq]``, packed ``[H, total_q]``)."""
     B, max_pages = block_table.shape
     num_pages, page_size, H, D = k_cache.shape
-    Sq = q.shape[0] // B
+    Sq = q.shape[0] // B if cu_seqlens_q is None else max_seqlen_q
     if scale is None:
         scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, H, Sq), device=q.device, dtype=torch.float32)
+        shape = (B, H, Sq) if cu_seqlens_q is None else (H, q.shape[0])
+        lse = torch.empty(shape, device=q.device, dtype=torch.float32)
     ws, ws_bytes = None, 0
     if num_splits != 1:
         ws_bytes = fa_fwd_splitkv_workspace_size(B, H, Sq, max_pages * page_size, D, num_splits)
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     fa_fwd_paged(q, k_cache, v_cache, block_table, seqlens_k, out, lse, B, H, Sq, D, num_pages, page_size, max_pages,
-                 scale, causal, num_splits, ws, ws_bytes, stream=stream)
+                 scale, causal, num_splits, ws, ws_bytes, cu_seqlens_q=cu_seqlens_q, total_q=q.shape[0],
+                 stream=stream)
     return out, lse

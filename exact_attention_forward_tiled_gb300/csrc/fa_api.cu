@@ -313,8 +313,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 
 int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
                  const int* seqlens_k, void* o, float* lse, int B, int H, int Sq, int D, int num_pages,
-                 int page_size, int max_pages, float scale, int causal, int num_splits, void* workspace,
-                 size_t workspace_bytes, int dtype, void* stream) {
+                 int page_size, int max_pages, float scale, int causal, const int* cu_seqlens_q, int total_q,
+                 int num_splits, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
   // ---- host-side checks of the paging arguments (the rest: setup_fwd16)
   if (num_pages <= 0 || max_pages <= 0 || B < 0) return FA_ERR_INVALID_ARG;
   if (!(page_size == 16 || page_size == 32 || page_size == 64 || (page_size > 0 && page_size % 128 == 0)))
@@ -326,14 +326,20 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
   if (B > 0 && (!block_table || !seqlens_k)) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(block_table) & 3u || reinterpret_cast<uintptr_t>(seqlens_k) & 3u)
     return FA_ERR_ALIGNMENT;
+  // packed queries: one launch (the key-range merge assumes fixed lengths)
+  const bool varlen_q = cu_seqlens_q != nullptr;
+  if (varlen_q && num_splits != 1) return FA_ERR_UNSUPPORTED;
+  if (varlen_q && total_q < 0) return FA_ERR_INVALID_ARG;
   fa::FwdLaunch L;
   DevInfo* dev = nullptr;
   bool nothing = false;
-  // the contiguous setup with K/V as one sequence of rows; the K/V maps are
-  // replaced below by maps over the whole caches
-  int st = setup_fwd16(L, &dev, &nothing, q, k_cache, v_cache, o, lse, B, H, Sq, 0, D, scale, causal, nullptr,
-                       nullptr, 0, 0, dtype, stream);
+  // the contiguous setup (queries fixed-length or packed; the packed form
+  // passes cu_seqlens_q for both sides, since the key side's offsets are
+  // unused here); the K/V maps are replaced below by maps over the caches
+  int st = setup_fwd16(L, &dev, &nothing, q, k_cache, v_cache, o, lse, B, H, Sq, 0, D, scale, causal,
+                       cu_seqlens_q, cu_seqlens_q, varlen_q ? total_q : 0, 0, dtype, stream);
   if (st != FA_OK || nothing) return st;
+  L.p.cu_k = nullptr;
   const CUtensorMapDataType dt = dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t cols = (uint64_t)H * D, rows = (uint64_t)num_pages * page_size;

@@ -148,12 +148,18 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   t.b = bh / p.H;
   t.h = bh - t.b * p.H;
   if (p.block_table != nullptr) {
-    // paged K/V: fixed query length, keys from seqlens_k through the block table
-    t.qtok = t.b * p.Sq;
+    // paged K/V: keys from seqlens_k through the block table; queries of a
+    // fixed length, or packed by cu_q
+    int qs = t.b * p.Sq, qe = qs + p.Sq;
+    if (p.cu_q != nullptr) {
+      qs = __ldg(p.cu_q + t.b);
+      qe = __ldg(p.cu_q + t.b + 1);
+    }
+    t.qtok = qs;
     t.ktok = 0;
-    t.Lq = p.Sq;
+    t.Lq = qe - qs;
     t.Lk = __ldg(p.seqlens_k + t.b);
-    if (t.Lk < 0 || t.Lk > p.Sk) {
+    if (qs < 0 || qe < qs || qe > p.total_q || t.Lq > p.Sq || t.Lk < 0 || t.Lk > p.Sk) {
       t.Lq = 0;
       t.Lk = 0;
       if (qblk == 0) atomicOr(p.status, kDevBadSeqlens);

@@ -139,22 +139,28 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
  * attention; here the kernel's TMA loads read each page in place, so there
  * is no gather pass and no extra copy.
  *
- *   q            [B*Sq, H, D] (fixed query length Sq per sequence)
+ *   q            [B*Sq, H, D] (fixed query length Sq per sequence), or
+ *                packed [total_q, H, D] when cu_seqlens_q is given
  *   k_cache, v_cache  [num_pages, page_size, H, D], same 16-bit type as q
  *   block_table  device int32 [B, max_pages]: page of each page_size-key
  *                block of each sequence
  *   seqlens_k    device int32 [B]: keys of each sequence (<= max_pages *
  *                page_size); key j of sequence b is row j % page_size of
  *                page block_table[b][j / page_size]
- *   o, lse       as fa_fwd with fixed length ([B*Sq, H, D], [B, H, Sq])
+ *   o, lse       as fa_fwd: [B*Sq, H, D] and [B, H, Sq], or with packed
+ *                queries [total_q, H, D] and [H, total_q]
+ *   cu_seqlens_q device int32 [B + 1] query prefix sums (Sq then bounds every
+ *                query length), or NULL for fixed-length queries; total_q =
+ *                rows of q. Packed queries take num_splits = 1
+ *                (FA_ERR_UNSUPPORTED otherwise).
  *   page_size    16, 32, 64 or a multiple of 128
  *   num_splits   key ranges as fa_fwd_splitkv: 1 = none (workspace unused),
  *                0 = automatic, > 1 = that many; the workspace is
  *                fa_fwd_splitkv_workspace_size(B, H, Sq, max_pages *
  *                page_size, D, num_splits) bytes when more than one range
  *                is used (NULL allowed otherwise)
- *   causal       bottom-right aligned per sequence (the Sq queries are the
- *                last Sq positions of a sequence of seqlens_k[b] keys)
+ *   causal       bottom-right aligned per sequence (a sequence's queries
+ *                are the last positions of its seqlens_k[b] keys)
  *
  * Only the table entries of a sequence's first ceil(seqlens_k[b] /
  * page_size) blocks are read. Every row of those pages must hold finite
@@ -168,6 +174,7 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
                  const int* seqlens_k, void* o, float* lse, int B, int H, int Sq, int D,
                  int num_pages, int page_size, int max_pages, float scale, int causal,
+                 const int* cu_seqlens_q, int total_q,
                  int num_splits, void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*

@@ -142,3 +142,43 @@ def test_paged_host_checks():
     st = api.fa_fwd_paged(q, kc, vc, None, seqlens, o, lse, 1, H, Sq, D, kc.shape[0], 32, table.shape[1], 0.125, 0,
                           check=False)
     assert st == -1
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_packed_queries(causal):
+    """Chunked prefill: a different number of new queries per sequence
+    (packed by cu_seqlens_q) against paged contexts; equal, bit for bit, to
+    the contiguous varlen path on the gathered keys."""
+    H, D, ps = 2, 128, 16
+    lq, lk = [5, 130, 1, 0, 64], [300, 200, 1, 50, 1000]
+    _, k, v, kc, vc, table, seqlens = _paged_problem(lk, 1, H, D, ps, torch.bfloat16, seed=60 + causal)
+    g = torch.Generator(device="cuda").manual_seed(61)
+    q = torch.randn((sum(lq), H, D), generator=g, device="cuda").to(torch.bfloat16)
+    cq = torch.tensor(np.concatenate([[0], np.cumsum(lq)]), dtype=torch.int32, device="cuda")
+    ck = torch.tensor(np.concatenate([[0], np.cumsum(lk)]), dtype=torch.int32, device="cuda")
+    o, lse = api.attention_forward_paged(q, kc, vc, table, seqlens, causal=causal, cu_seqlens_q=cq,
+                                         max_seqlen_q=max(lq))
+    api.fa_get_device_status()
+    o_ref, lse_ref = orc.attention(q.cpu(), k.cpu(), v.cpu(), scale=D ** -0.5, causal=causal, nseq=len(lq),
+                                   cu_seqlens_q=cq.cpu().numpy(), cu_seqlens_k=ck.cpu().numpy())
+    _check_vs_oracle(o, lse, o_ref, lse_ref, torch.bfloat16)
+    o2, lse2 = api.attention_forward(q, k, v, causal=causal, cu_seqlens_q=cq, cu_seqlens_k=ck,
+                                     max_seqlen_q=max(lq), max_seqlen_k=max(lk))
+    api.fa_get_device_status()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    # packed queries take one launch: key ranges are refused
+    st = api.fa_fwd_paged(q, kc, vc, table, seqlens, o, lse, len(lq), H, max(lq), D, kc.shape[0], ps,
+                          table.shape[1], D ** -0.5, causal, num_splits=2, cu_seqlens_q=cq, total_q=q.shape[0],
+                          check=False)
+    assert st == -2
+
+
+def test_paged_key_ranges_with_several_queries():
+    """Key ranges with more than one query row per sequence (causal): the
+    merge of the ranges equals the oracle."""
+    lens, Sq, H, D = [900, 1500, 70], 70, 2, 128
+    q, k, v, kc, vc, table, seqlens = _paged_problem(lens, Sq, H, D, 32, torch.bfloat16, seed=70)
+    o, lse = api.attention_forward_paged(q, kc, vc, table, seqlens, causal=True, num_splits=3)
+    api.fa_get_device_status()
+    o_ref, lse_ref = _oracle(q, k, v, lens, Sq, D ** -0.5, True)
+    _check_vs_oracle(o, lse, o_ref, lse_ref, torch.bfloat16)
