@@ -217,10 +217,12 @@ __device__ __forceinline__ int fetch_tile(const FwdParams& p, int j) {
 }
 
 // ------------------------------------------------------------------ load warp
-// The whole warp runs this role. Lane 0 does the waits, the tile ring and the
-// contiguous TMA loads; for paged K/V every lane s < 128 / page_rows looks up,
-// and loads, box s of a tile itself, so a tile's block-table reads and copies
-// are issued in parallel rather than one after another.
+// Contiguous K/V: lane 0 alone runs this role. Paged K/V: the whole warp runs
+// it; lane 0 does the waits, the tile ring and the Q loads, and every lane
+// s < 128 / page_rows looks up, and loads, box s of a tile itself, so a tile's
+// block-table reads and copies are issued in parallel rather than one after
+// another. (The idle lanes would cost the contiguous one-tile configuration
+// issue slots, measured 6 % at D = 256, so they stay out of it.)
 template <class C, bool CAUSAL>
 __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                           const FwdParams& p, uint32_t sbase, const Waiter& wt, const TileRing& ring) {
@@ -228,13 +230,15 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   auto bar = [&](int i) { return bars + 8u * i; };
   const int lane = threadIdx.x & 31;
   const bool lead = lane == 0;
+  const bool paged = p.block_table != nullptr;
+  const unsigned lanes = paged ? 0xffffffffu : 1u;   // the lanes running this role
   uint32_t kvc = 0, tcount = 0;
   bool ok = true;
-  // lane 0 waits; every lane learns the outcome
+  // lane 0 waits; every participating lane learns the outcome
   auto wait0 = [&](uint32_t b, uint32_t parity, int where) -> bool {
     bool r = true;
     if (lead) r = wt.wait(b, parity, where);
-    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    return __shfl_sync(lanes, r ? 1 : 0, 0) != 0;
   };
 
   auto load_tile = [&](const CUtensorMap* m, int h, int row, uint32_t dst, uint32_t b) {
@@ -249,7 +253,6 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   // issues the lane's block-table read before lane 0 waits for a free slot,
   // page_rows turns it into a row after the wait, so the read's latency hides
   // behind the wait. Page sizes that are powers of two divide by shifting.
-  const bool paged = p.block_table != nullptr;
   const int nsub = paged ? 128 / p.page_rows : 0;
   const bool my_box = lane < nsub;
   int tag_a = -1, tag_b = -1;       // pack_tag of the cached blocks
@@ -304,7 +307,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
       // 2 KB boundary of the swizzled tile. The expected byte count is set
       // before any lane's copy is issued.
       const int row = page_rows(kb);
-      __syncwarp();
+      __syncwarp(lanes);
       if (my_box) {
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
@@ -325,7 +328,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
       ring.slots[rs] = w;
       ptx::mbar_arrive(ring.full(rs));
     }
-    w = __shfl_sync(0xffffffffu, w, 0);
+    w = __shfl_sync(lanes, w, 0);
     if (w < 0) break;
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
@@ -808,7 +811,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kRebalance) ptx::setmaxnreg_dec<C::kRegsLow>();
     if (warp == C::kLoadWarp) {
-      load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
+      if (p.block_table != nullptr || lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
     } else if (warp == C::kMmaWarp) {
       if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt, ring);
     }
