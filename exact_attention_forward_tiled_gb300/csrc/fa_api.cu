@@ -225,16 +225,39 @@ int launch16(fa::FwdLaunch& L, DevInfo* dev) {
   return FA_OK;
 }
 
-// Key ranges of the split-KV forward: `requested` <= 0 picks enough ranges for
-// about two work tiles per SM. Returns the ranges actually used (every range
-// non-empty) and their length in 128-key blocks.
+// Key ranges of the split-KV forward. `requested` > 0 asks for that many;
+// `requested` <= 0 picks the count with the least estimated time, counting
+// whole waves of work tiles over the SMs times the 128-key blocks of one tile
+// plus a per-tile overhead of about four blocks (Q load, pipeline fill,
+// partial-result write), fewer ranges on ties. Work tiles come in whole
+// waves, so 9 ranges of 57 blocks in one wave beat 10 ranges in two.
+// Returns the ranges actually used (every range non-empty) and their length
+// in 128-key blocks.
 void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms, int* n_split,
                     int* split_blocks) {
   const int64_t nblocks = ((int64_t)Sk + 127) / 128;
   const int rows = fa::cta_rows16(D, Sq);
   const int64_t tiles = (int64_t)B * H * (((int64_t)Sq + rows - 1) / rows);
   int64_t n = requested;
-  if (n <= 0) n = tiles > 0 ? (2 * (int64_t)sms + tiles - 1) / tiles : 1;
+  if (n <= 0) {
+    n = 1;
+    if (tiles > 0 && sms > 0) {
+      const int64_t kOverhead = 4;
+      int64_t best = -1;
+      const int64_t top = nblocks < kMaxSplits ? nblocks : kMaxSplits;
+      for (int64_t c = 1; c <= top; ++c) {
+        const int64_t per = (nblocks + c - 1) / c;
+        const int64_t used = (nblocks + per - 1) / per;   // non-empty ranges
+        if (used != c) continue;
+        const int64_t waves = (tiles * c + sms - 1) / sms;
+        const int64_t cost = waves * (per + kOverhead);
+        if (best < 0 || cost < best) {
+          best = cost;
+          n = c;
+        }
+      }
+    }
+  }
   if (n > kMaxSplits) n = kMaxSplits;
   if (n > nblocks) n = nblocks;
   if (n < 1) n = 1;
