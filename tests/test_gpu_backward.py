@@ -220,3 +220,28 @@ def test_backward_full_size_sampled(name):
             err = np.abs(orc._f64(got.cpu()) - ref)
             ratio = (err / (2.0 * bd + 1e-6)).max()
             assert ratio <= 1.0, (name, b, h, float(ratio), float(err.max()))
+
+
+@pytest.mark.parametrize("scale", [0.0, 1.0])
+def test_backward_extreme_scales(scale):
+    """scale 0: uniform P, dQ = dK = 0 and dV = the mean of dO; scale 1 at
+    D = 128: a peaked softmax, where P and dS rounding matter most. Both
+    under the element-wise bound."""
+    B, H, S, D = 1, 2, 300, 128
+    q, k, v, do = (_rand((B * S, H, D), torch.bfloat16, 400 + i) for i in range(4))
+    o, lse = api.attention_forward(q, k, v, causal=True, scale=scale, batch=B)
+    dq, dk, dv = api.attention_backward(q, k, v, o, lse, do, causal=True, scale=scale, batch=B)
+    api.fa_get_device_status()
+    qn, kn, vn, don = (orc._f64(t.cpu()) for t in (q, k, v, do))
+    rq, rk, rv = orc.attention_backward(qn, kn, vn, don, scale=scale, causal=True, nseq=B, Sq=S, Sk=S)
+    _, lse_ref = orc.attention(qn, kn, vn, scale=scale, causal=True, nseq=B, Sq=S, Sk=S)
+    eps = np.abs(lse.cpu().numpy() - lse_ref).max() + 2.0 ** -21
+    o16 = orc._f64(o.cpu())
+    for h in range(H):
+        bq, bk, bv = _bounds_head(qn[:, h], kn[:, h], vn[:, h], don[:, h], o16[:, h], scale, True, 2.0 ** -8, eps)
+        for name, got, ref, bd in (("dQ", dq[:, h], rq[:, h], bq), ("dK", dk[:, h], rk[:, h], bk),
+                                   ("dV", dv[:, h], rv[:, h], bv)):
+            err = np.abs(orc._f64(got.cpu()) - ref)
+            assert (err <= 2.0 * bd + 1e-6).all(), (name, h, float(err.max()))
+    if scale == 0.0:
+        assert int(dq.abs().sum().item()) == 0 and int(dk.abs().sum().item()) == 0
