@@ -7,14 +7,17 @@
 //
 // Persistent CTAs walk the 128 x D blocks (one head of one tensor each); a
 // TMA copy brings the next block into shared memory while the current one is
-// rotated in registers (butterflies over the bits of d inside a lane, then
-// across lanes with shuffles), its amax is reduced through shared memory and
-// its codes are written, so every element is read from HBM once and written
-// once, with reads in flight throughout.
+// rotated in registers, its amax is reduced through shared memory and its
+// codes are written, so every element is read from HBM once and written once,
+// with reads in flight throughout. For D <= 128 a thread owns a whole row and
+// runs its Walsh-Hadamard transform on packed fp32 pairs without any
+// cross-lane traffic (fp8_prep_rows_kernel); D = 256 spreads a row over 32
+// lanes and finishes the transform with shuffles (fp8_prep_lanes_kernel).
 #include <cstdint>
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "pipeline.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -85,7 +88,7 @@ __device__ __forceinline__ bool prep_block(const PrepBatch& pb, int bid, PrepBlo
   return true;
 }
 
-// Persistent CTAs, each walking blocks bid = blockIdx.x, + gridDim.x, ...
+// D = 256. Persistent CTAs, each walking blocks bid = blockIdx.x, + gridDim.x, ...
 // A block is 128 rows x D of one head of one tensor. Thread 0 fetches the
 // next block with one TMA copy into the other half of a shared-memory double
 // buffer while the CTA works on the current one, so HBM reads stay in flight
@@ -98,7 +101,7 @@ __device__ __forceinline__ bool prep_block(const PrepBatch& pb, int bid, PrepBlo
 // are written with 8-byte stores.
 template <int D>
 __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2)
-    fp8_prep_kernel(const __grid_constant__ PrepMaps maps, const PrepBatch pb, int total_blocks) {
+    fp8_prep_lanes_kernel(const __grid_constant__ PrepMaps maps, const PrepBatch pb, int total_blocks) {
   constexpr int NW = D == 256 ? 32 : 16;  // warps per CTA
   constexpr int LPR = D / 8;               // lanes per row
   constexpr int RPI = 32 / LPR;            // rows per warp instruction
@@ -243,6 +246,221 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2)
   }
 }
 
+// ------------------------------------------------------------ D <= 128
+// Two 16-bit elements -> fp32 (bf16: the bits shifted into place; fp16: the
+// hardware conversion).
+template <bool BF16>
+__device__ __forceinline__ void cvt2(uint32_t w, float& lo, float& hi) {
+  if (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
+  }
+}
+
+// Offset of byte `o` of a block laid out row-major in shared memory by a TMA
+// copy with the 128-byte swizzle (16-byte unit bits 4..6 XOR address bits
+// 7..9) or the 64-byte one (bits 4..5 XOR bits 7..8).
+template <int SW>
+__device__ __forceinline__ uint32_t swizzled(uint32_t o) {
+  return o ^ (((o >> 7) & (SW == 128 ? 7u : 3u)) << 4);
+}
+
+// Row r of a 128 x D block (D / 64 input boxes of 64 elements x 128 rows,
+// 128-byte swizzle) into v: v[i] holds elements 2i and 2i + 1. With ROT the
+// row gets its sign flips (XOR of the sign bits, bit 15 of each 16-bit
+// element, by mask) and the whole D-point Walsh-Hadamard transform: the
+// butterfly over bit 0 of d pairs the two halves of a packed register, every
+// other bit pairs two registers, so all but the first stage are f32x2 adds and
+// subtracts. Returns max |x| over the row.
+template <int D, bool ROT, bool BF16>
+__device__ __forceinline__ float load_row(const uint8_t* blk, int r, const uint32_t* mask, uint64_t (&v)[D / 2]) {
+  constexpr int NP = D / 2;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint32_t off = (uint32_t)(c / 8) * 16384u + swizzled<128>((uint32_t)r * 128u + (uint32_t)(c % 8) * 16u);
+    uint4 u = *reinterpret_cast<const uint4*>(blk + off);
+    if (ROT) {
+      const uint4 m = *reinterpret_cast<const uint4*>(mask + 4 * c);
+      u.x ^= m.x;
+      u.y ^= m.y;
+      u.z ^= m.z;
+      u.w ^= m.w;
+    }
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a, b;
+      cvt2<BF16>(w[j], a, b);
+      v[4 * c + j] = ROT ? ptx::f2pack(a + b, a - b) : ptx::f2pack(a, b);
+    }
+  }
+  if (ROT) {
+#pragma unroll
+    for (int st = 1; st < NP; st <<= 1) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        if (i & st) continue;
+        const uint64_t a = v[i], b = v[i | st];
+        v[i] = ptx::add2(a, b);
+        v[i | st] = ptx::sub2(a, b);
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    float a, b;
+    ptx::f2unpack(v[i], a, b);
+    amax = ptx::max3(amax, fabsf(a), fabsf(b));
+  }
+  return amax;
+}
+
+// D = 64, 128. Persistent CTAs of 128 threads walk the blocks; thread r owns
+// row r of the current block. Thread 0 keeps the next block's TMA copy in
+// flight (two shared-memory buffers) while the CTA rotates the current one in
+// registers; the block amax goes through one CTA barrier; the codes of a full
+// block are written back into its buffer (its input has been read by then)
+// and leave with one TMA store, those of a ragged last block with plain
+// stores of the valid rows.
+template <int D>
+__global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
+    fp8_prep_rows_kernel(const __grid_constant__ PrepMaps in_maps, const __grid_constant__ PrepMaps out_maps,
+                         const PrepBatch pb, int total_blocks) {
+  constexpr int NP = D / 2;
+  constexpr uint32_t kBlockBytes = 128u * D * 2u;
+  constexpr int kOutSwizzle = D == 128 ? 128 : 64;   // the output map's swizzle (rows of D bytes)
+  extern __shared__ uint8_t prep_raw[];
+  __shared__ float red[4];
+  __shared__ __align__(8) uint64_t full_bar[2];
+  __shared__ __align__(16) uint32_t smask[3][NP];
+  __shared__ int gave_up;
+  // 1024-byte aligned buffers (the swizzle pattern repeats every 1024 bytes)
+  const uint32_t raw = ptx::smem_u32(prep_raw);
+  const uint32_t buf0 = (raw + 1023u) & ~1023u;
+  uint8_t* const buf0_ptr = prep_raw + (buf0 - raw);
+  const uint32_t bar0 = ptx::smem_u32(&full_bar[0]);
+  const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+
+  // sign masks of each tensor's sigma (+-1), two elements per word
+  for (int i = threadIdx.x; i < 3 * NP; i += blockDim.x) {
+    const int ti = i / NP, j = i % NP;
+    const int8_t* sg = ti < pb.n ? pb.t[ti].sigma : nullptr;
+    smask[ti][j] = sg != nullptr ? (sg[2 * j] < 0 ? 0x8000u : 0u) | (sg[2 * j + 1] < 0 ? 0x80000000u : 0u) : 0u;
+  }
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar0, 1);
+    ptx::mbar_init(bar0 + 8u, 1);
+    ptx::fence_mbar_init();
+    gave_up = 0;
+  }
+  __syncthreads();
+  const Waiter wt{&gave_up, nullptr};
+
+  // thread 0: fetch block `bid` into buffer `s` (nothing if it is skipped)
+  auto fetch = [&](int bid, int s) -> bool {
+    PrepBlock pbk;
+    if (bid >= total_blocks || !prep_block(pb, bid, pbk)) return false;
+    const uint32_t bar = bar0 + 8u * s;
+    ptx::mbar_arrive_expect_tx(bar, kBlockBytes);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      ptx::tma_load_2d(buf0 + s * kBlockBytes + c * 16384u, &in_maps.m[pbk.ti], pbk.h * D + c * 64,
+                       (int)(pbk.start + pbk.blk * 128), bar);
+    return true;
+  };
+  uint32_t pending = 0u;              // thread 0, bit i: a copy into buffer i is in flight
+  if (threadIdx.x == 0 && fetch(blockIdx.x, 0)) pending = 1u;
+  uint32_t phase_bits = 0u;           // bit i: parity of buffer i's next completion
+
+  int s = 0;
+  for (int bid = blockIdx.x; bid < total_blocks; bid += gridDim.x, s ^= 1) {
+    PrepBlock pbk;
+    const bool live = prep_block(pb, bid, pbk);
+    if (threadIdx.x == 0) {
+      // the other buffer last held the previous block's codes: its store
+      // must have read them before the next block is copied in
+      ptx::bulk_wait_read_all();
+      if (fetch(bid + gridDim.x, s ^ 1)) pending |= 1u << (s ^ 1);
+    }
+    if (!live) continue;
+    const PrepParams& P = pb.t[pbk.ti];
+    Waiter w = wt;
+    w.status = P.status;
+    const bool ok = w.wait(bar0 + 8u * s, (phase_bits >> s) & 1u, 0x40);
+    phase_bits ^= 1u << s;
+    pending &= ~(1u << s);
+    const int valid = min(128, pbk.L - pbk.blk * 128);
+    uint8_t* const blk = buf0_ptr + s * kBlockBytes;
+
+    uint64_t v[NP];
+    float amax = 0.f;
+    if (ok && r < valid) {
+      const uint32_t* m = smask[pbk.ti];
+      if (P.sigma != nullptr)
+        amax = P.bf16 ? load_row<D, true, true>(blk, r, m, v) : load_row<D, true, false>(blk, r, m, v);
+      else
+        amax = P.bf16 ? load_row<D, false, true>(blk, r, m, v) : load_row<D, false, false>(blk, r, m, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) v[i] = 0ull;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    // CTA barrier (every thread has also read its row out of the buffer) that
+    // agrees on giving up if any thread's wait did
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        ptx::bulk_wait_all();
+        for (int i = 0; i < 2; ++i)
+          if ((pending >> i) & 1u) w.drain(bar0 + 8u * i, (phase_bits >> i) & 1u);
+      }
+      return;
+    }
+    // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
+    const float norm = P.sigma != nullptr ? rsqrtf((float)D) : 1.f;
+    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) * norm;
+    const float scale = amax > 0.f ? amax / 448.f : 1.f;
+    const float inv = norm / scale;
+    if (threadIdx.x == 0) P.scale[pbk.sidx] = scale;
+
+    uint32_t code[NP / 2];
+    const uint64_t inv2 = ptx::f2pack(inv, inv);
+#pragma unroll
+    for (int i = 0; i < NP; i += 2) {
+      float a0, a1, b0, b1;
+      ptx::f2unpack(ptx::mul2(v[i], inv2), a0, a1);
+      ptx::f2unpack(ptx::mul2(v[i + 1], inv2), b0, b1);
+      code[i / 2] = ptx::pack_e4m3x2(a0, a1) | (ptx::pack_e4m3x2(b0, b1) << 16);
+    }
+    const int row0 = pbk.blk * 128;
+    if (valid == 128) {
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c)
+        *reinterpret_cast<uint4*>(blk + swizzled<kOutSwizzle>((uint32_t)r * D + (uint32_t)c * 16u)) =
+            make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        ptx::tma_store_2d(&out_maps.m[pbk.ti], buf0 + s * kBlockBytes, pbk.h * D, (int)(pbk.start + row0));
+        ptx::bulk_commit();
+      }
+    } else if (r < valid) {
+      uint8_t* dst = P.x8 + ((pbk.start + row0 + r) * P.H + pbk.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c)
+        *reinterpret_cast<uint4*>(dst + 16 * c) =
+            make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+    }
+  }
+  if (threadIdx.x == 0) ptx::bulk_wait_all();
+}
+
 // cu_blocks[b] = sum over b' < b of ceil(L_b' / 128), L_b = cu_seqlens[b+1] - cu_seqlens[b]
 // (a negative length counts as 0). One thread: B is small next to the rest.
 __global__ void varlen_blocks_kernel(const int* __restrict__ cu_seqlens, int B, int* __restrict__ cu_blocks) {
@@ -261,42 +479,43 @@ cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* maps, int n_tensors, int D, int num_sms,
-                            cudaStream_t stream) {
+cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* in_maps, const CUtensorMap* out_maps,
+                            int n_tensors, int D, int num_sms, cudaStream_t stream) {
   PrepBatch pb{};
-  PrepMaps pm{};
+  PrepMaps pin{}, pout{};
   long total = 0;
   pb.n = n_tensors;
   for (int i = 0; i < n_tensors; ++i) {
     pb.t[i] = tensors[i];
-    pm.m[i] = maps[i];
+    pin.m[i] = in_maps[i];
+    if (D <= 128) pout.m[i] = out_maps[i];
     pb.count[i] = tensors[i].B * tensors[i].H * tensors[i].nblk;
     total += pb.count[i];
   }
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffL) return cudaErrorInvalidValue;
-  // resident CTAs: two per SM for D <= 128 (64 registers x 512 threads,
-  // kPrepBuffers 128-row blocks of shared memory each), one for D = 256
-  // (1024 threads)
-  const long per_sm = D == 256 ? 1L : 2L;
-  const int grid = (int)(total < per_sm * num_sms ? total : per_sm * num_sms);
-  const size_t smem = (size_t)kPrepBuffers * 128u * (size_t)D * 2u;
   cudaError_t e;
-  switch (D) {
-    case 64:
-      e = cudaFuncSetAttribute(fp8_prep_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) fp8_prep_kernel<64><<<grid, 32 * 16, smem, stream>>>(pm, pb, (int)total);
-      break;
-    case 128:
-      e = cudaFuncSetAttribute(fp8_prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) fp8_prep_kernel<128><<<grid, 32 * 16, smem, stream>>>(pm, pb, (int)total);
-      break;
-    case 256:
-      e = cudaFuncSetAttribute(fp8_prep_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) fp8_prep_kernel<256><<<grid, 32 * 32, smem, stream>>>(pm, pb, (int)total);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+  if (D == 64 || D == 128) {
+    // resident CTAs per SM: shared memory (two blocks of 128 x D 16-bit
+    // elements + alignment) and registers (a row of D fp32 per thread)
+    const long per_sm = D == 64 ? 5L : 3L;
+    const int grid = (int)(total < per_sm * num_sms ? total : per_sm * num_sms);
+    const size_t smem = 2u * 128u * (size_t)D * 2u + 1024u;
+    if (D == 64) {
+      e = cudaFuncSetAttribute(fp8_prep_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) fp8_prep_rows_kernel<64><<<grid, 128, smem, stream>>>(pin, pout, pb, (int)total);
+    } else {
+      e = cudaFuncSetAttribute(fp8_prep_rows_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) fp8_prep_rows_kernel<128><<<grid, 128, smem, stream>>>(pin, pout, pb, (int)total);
+    }
+  } else if (D == 256) {
+    // one resident CTA per SM (1024 threads, kPrepBuffers 128 x 256 blocks)
+    const int grid = (int)(total < num_sms ? total : num_sms);
+    const size_t smem = (size_t)kPrepBuffers * 128u * (size_t)D * 2u;
+    e = cudaFuncSetAttribute(fp8_prep_lanes_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) fp8_prep_lanes_kernel<256><<<grid, 32 * 32, smem, stream>>>(pin, pb, (int)total);
+  } else {
+    return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
