@@ -100,8 +100,8 @@ struct BwdTile {
 template <bool DQ, bool CAUSAL>
 __device__ __forceinline__ BwdTile bwd_tile(const BwdParams& p, int w) {
   BwdTile t;
-  const int bh = w / p.n_rblk;
-  const int j = w - bh * p.n_rblk;
+  int bh, j;
+  tile_order(w, p.n_rblk, p.B * p.H, p.head_group, bh, j);
   // causal: heavy tiles first (dQ: the last query blocks see the most keys;
   // dK/dV: the first key blocks are seen by the most queries)
   const int rblk = (DQ && CAUSAL) ? p.n_rblk - 1 - j : j;

@@ -112,6 +112,17 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Heads per tile group (fa::tile_order). Causal problems: as many heads as
+// keep the streamed side of the group (two tensors of stream_rows x D
+// elements per head) within about 32 MB of L2, 1 to 16; otherwise 1 (every
+// tile of a head costs the same, head by head keeps the L2 footprint least).
+int head_group(bool causal, int64_t BH, int64_t stream_rows, int D, int elem_bytes) {
+  if (!causal) return 1;
+  const int64_t per_head = std::max<int64_t>(stream_rows * D * elem_bytes * 2, 1);
+  const int64_t fit = ((int64_t)32 << 20) / per_head;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(BH, 16), fit));
+}
+
 }  // namespace
 
 extern "C" {
@@ -212,6 +223,7 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
 
 int launch16(fa::FwdLaunch& L, DevInfo* dev) {
   L.p.sched = dev->take_slot();
+  L.p.head_group = head_group(L.causal, (int64_t)L.p.B * L.p.H, L.p.Sk, L.D, 2);
   cudaError_t e;
   switch (L.D) {
     case 64: e = L.one_tile ? fa::launch_fwd_d64_q1(L) : fa::launch_fwd_d64(L); break;
@@ -549,6 +561,7 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   L.D = D;
   L.kind = fa::kE4M3;
   L.causal = causal != 0;
+  L.p.head_group = head_group(L.causal, (int64_t)B * H, Sk, D, 1);
   L.num_sms = dev->sms;
   L.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = D == 128 ? fa::launch_fwd_fp8_d128(L) : fa::launch_fwd_fp8_d256(L);
@@ -693,6 +706,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
     L.causal = causal != 0;
     L.dq = dqk;
+    L.p.head_group = head_group(L.causal, (int64_t)B * H, dqk ? Sk : Sq, D, 2);
     L.num_sms = dev->sms;
     L.stream = s;
     if (L.p.ntiles == 0) continue;

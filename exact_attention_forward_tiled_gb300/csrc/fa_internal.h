@@ -58,7 +58,29 @@ struct FwdParams {
   int max_pages, page_size, num_pages, page_rows;
   int page_shift;   // log2(page_size) for a power of two, else -1
   int n_kblk_tag;   // max_pages * page_size / 128 + 1: tags a (sequence, key block) pair
+  int head_group;   // heads whose tiles are visited rank-major together (tile_order)
 };
+
+// Work tile w -> (sequence-head index bh, rank jj of the tile within its
+// head) for B*H heads of per_head tiles each. Heads go in groups of G; within
+// a group the tiles are taken rank by rank (rank 0 of every head of the group,
+// then rank 1, ...), so with ranks ordered from the most expensive tile down
+// (causal) the last tiles handed out are the cheapest ones and the run ends
+// without a long tile running alone, while the heads in flight at one time
+// (about one group) keep their streamed K/V in L2. G = 1: head by head.
+// A bijection of [0, BH * per_head) for every G >= 1.
+__host__ __device__ inline void tile_order(int w, int per_head, int BH, int G, int& bh, int& jj) {
+  if (G <= 1) {
+    bh = w / per_head;
+    jj = w - bh * per_head;
+    return;
+  }
+  const int g0 = (w / (G * per_head)) * G;        // first head of w's group
+  const int gn = BH - g0 < G ? BH - g0 : G;        // heads in that group
+  const int r = w - g0 * per_head;
+  jj = r / gn;
+  bh = g0 + (r - jj * gn);
+}
 
 // Element kinds of the attention inputs.
 enum Kind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
@@ -112,6 +134,7 @@ struct BwdParams {
   float scale;             // softmax scale (the factor of dQ and dK)
   int* status;
   unsigned int* sched;
+  int head_group;          // heads whose tiles are visited rank-major together (tile_order)
 };
 
 struct BwdLaunch {

@@ -132,15 +132,16 @@ struct TileInfo {
   bool live;       // false: the block starts beyond the sequence
 };
 
-// Heads are the outer loop so that the CTAs running at the same time share
-// their K/V through L2; under the causal mask the blocks of a head are
-// visited from the most expensive (last rows) to the cheapest.
+// Heads are the outer loop (in groups of p.head_group, tile_order) so that
+// the CTAs running at the same time share their K/V through L2; under the
+// causal mask the blocks of a head are ranked from the most expensive (last
+// rows) to the cheapest.
 template <int ROWS, bool CAUSAL>
 __device__ __forceinline__ TileInfo tile_info(const FwdParams& p, int w) {
   TileInfo t;
   const int per_head = p.n_qblk * p.n_split;
-  const int bh = w / per_head;
-  const int jj = w - bh * per_head;
+  int bh, jj;
+  tile_order(w, per_head, p.B * p.H, p.head_group, bh, jj);
   const int j = jj / p.n_split;
   t.split = jj - j * p.n_split;
   const int qblk = CAUSAL ? (p.n_qblk - 1 - j) : j;
