@@ -235,11 +235,9 @@ __global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2)
     for (int i = 0; i < ITER; ++i) {
       const int row = pbk.blk * 128 + warp * RPW + i * RPI + sub;
       if (row >= pbk.L) continue;
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = ptx::pack_e4m3x2(x[i][2 * j] * inv, x[i][2 * j + 1] * inv);
       *reinterpret_cast<uint2*>(P.x8 + ((pbk.start + row) * P.H + pbk.h) * D + d0) =
-          make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+          make_uint2(ptx::pack_e4m3x4(x[i][0] * inv, x[i][1] * inv, x[i][2] * inv, x[i][3] * inv),
+                     ptx::pack_e4m3x4(x[i][4] * inv, x[i][5] * inv, x[i][6] * inv, x[i][7] * inv));
     }
     // red[] and this buffer are reused by the next iterations
     __syncthreads();
@@ -436,7 +434,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
       float a0, a1, b0, b1;
       ptx::f2unpack(ptx::mul2(v[i], inv2), a0, a1);
       ptx::f2unpack(ptx::mul2(v[i + 1], inv2), b0, b1);
-      code[i / 2] = ptx::pack_e4m3x2(a0, a1) | (ptx::pack_e4m3x2(b0, b1) << 16);
+      code[i / 2] = ptx::pack_e4m3x4(a0, a1, b0, b1);
     }
     const int row0 = pbk.blk * 128;
     if (valid == 128) {

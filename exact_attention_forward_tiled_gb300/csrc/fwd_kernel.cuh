@@ -27,7 +27,9 @@
 //   load warp (one thread)
 //       TMA loads of the Q tiles and of K_j, V_j into a ring of shared-memory
 //       slots guarded by full / empty mbarriers (producer / consumer of the
-//       wiki's technique 1; multi-stage K/V pipeline of technique 2).
+//       wiki's technique 1; multi-stage K/V pipeline of technique 2). Paged
+//       K/V: two whole warps, one for Q and K, one for V (a block of small
+//       pages is many small copies, and one warp issues them one at a time).
 //
 // Input kinds: fp16 or bf16 (tcgen05 kind::f16, 16 keys per MMA step), or
 // e4m3 with per-128-row-block scales (kind::f8f6f4, 32 keys per step; the
@@ -84,12 +86,13 @@ struct FwdCfg {
   static constexpr int kSoftmaxWarps = 4 * QT;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kLoadWarp = kSoftmaxWarps + 1;
-  // QT = 2: a third warpgroup (MMA warp, load warp, two idle warps) gives its
-  // registers to the two softmax warpgroups: 384 threads launch at 168
-  // registers each (64512); 128 x 64 + 256 x 216 = 63488 <= 64512.
+  static constexpr int kVLoadWarp = kSoftmaxWarps + 2;   // paged K/V only: the V loads
+  // QT = 2: a third warpgroup (MMA warp, load warp, V-load warp, one idle
+  // warp) gives its registers to the two softmax warpgroups: 384 threads
+  // launch at 168 registers each (64512); 128 x 64 + 256 x 216 = 63488 <= 64512.
   static constexpr bool kRebalance = QT == 2;
   static constexpr int kRegsLow = 64, kRegsHigh = 216;
-  static constexpr int kThreads = kRebalance ? 384 : 32 * (kSoftmaxWarps + 2);
+  static constexpr int kThreads = kRebalance ? 384 : 32 * (kSoftmaxWarps + 3);
   static_assert(!kRebalance || kThreads * 168 >= 128 * kRegsLow + 256 * kRegsHigh, "register split");
   static constexpr int kTmemCols = 512;
   // tensor-memory columns: score buffers S0, S1; accumulators O0 (, O1)
@@ -109,7 +112,8 @@ struct FwdCfg {
                        kBarOFull = kBarPFull + 4, kBarPVDone = kBarOFull + 2,
                        kBarMmaDone = kBarPVDone + 1, kBarTileFull = kBarMmaDone + 1,
                        kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
-  static constexpr int kTileConsumers = 1 + kSoftmaxWarps;  // MMA thread + one lane per softmax warp
+  // MMA thread + one lane per softmax warp (+ the V-load warp with paged K/V)
+  static constexpr int kTileConsumers = 1 + kSoftmaxWarps;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem address, abort flag, tile ring
   static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
 
@@ -218,22 +222,30 @@ __device__ __forceinline__ int fetch_tile(const FwdParams& p, int j) {
 }
 
 // ------------------------------------------------------------------ load warp
-// Contiguous K/V: lane 0 alone runs this role. Paged K/V: the whole warp runs
-// it; lane 0 does the waits, the tile ring and the Q loads, and every lane
-// s < 128 / page_rows looks up, and loads, box s of a tile itself, so a tile's
-// block-table reads and copies are issued in parallel rather than one after
-// another. (The idle lanes would cost the contiguous one-tile configuration
-// issue slots, measured 6 % at D = 256, so they stay out of it.)
-template <class C, bool CAUSAL>
+// MODE 0, contiguous K/V: lane 0 of the load warp alone runs this role (the
+// idle lanes would cost the contiguous one-tile configuration issue slots,
+// measured 6 % at D = 256). Paged K/V: two whole warps, MODE 1 (the load
+// warp: work tiles into the ring, Q, K) and MODE 2 (the V-load warp: takes
+// the work tiles from the ring like the other consumers, loads V). In each,
+// lane 0 does the waits and every lane s < 128 / page_rows looks up, and
+// loads, box s of a tile itself, so a tile's block-table reads and copies are
+// issued in parallel. Each warp issues its copies one after another (about 55
+// cycles each, measured), so at 16-row pages one warp for both K and V was the
+// limit. Both paged warps walk the same ring-slot sequence (K0, V0, K1, ... or
+// K0, K1, V0, K2, ...) and act on their own tensor's slots only; every fill
+// of a slot waits for the consumption of the one before it.
+template <class C, bool CAUSAL, int MODE>
 __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                           const FwdParams& p, uint32_t sbase, const Waiter& wt, const TileRing& ring) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   const int lane = threadIdx.x & 31;
   const bool lead = lane == 0;
-  const bool paged = p.block_table != nullptr;
+  constexpr bool paged = MODE != 0;
+  constexpr bool do_k = MODE != 2, do_v = MODE != 1;
   const unsigned lanes = paged ? 0xffffffffu : 1u;   // the lanes running this role
   uint32_t kvc = 0, tcount = 0;
+  uint32_t acted = 0;   // bit i: this warp filled slot kvc - 1 - i
   bool ok = true;
   // lane 0 waits; every participating lane learns the outcome
   auto wait0 = [&](uint32_t b, uint32_t parity, int where) -> bool {
@@ -291,8 +303,14 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
     }
     return row;
   };
-  // K or V tile of 128-key block kb (absolute within the sequence)
-  auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb) -> bool {
+  // K or V tile of 128-key block kb (absolute within the sequence); a tile
+  // of the other paged warp's tensor only takes its place in the slot order
+  auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb, bool act) -> bool {
+    acted = (acted << 1) | (act ? 1u : 0u);
+    if (!act) {
+      ++kvc;
+      return true;
+    }
     const int s = kvc % C::STAGES;
     const uint32_t ph = (kvc / C::STAGES) & 1u;
     if (paged) page_fetch(ti, kb);
@@ -321,51 +339,60 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   };
 
   for (int j = 0; ok; ++j) {
-    const int rs = j % C::kTileRing;
-    if (!wait0(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 9)) break;
     int w = 0;
-    if (lead) {
-      w = fetch_tile<C::kTileRing>(p, j);
-      ring.slots[rs] = w;
-      ptx::mbar_arrive(ring.full(rs));
+    if (MODE == 2) {
+      // the V-load warp takes the work tiles from the ring
+      if (!next_tile(ring, wt, j, C::kTileRing, true, lead, w)) break;
+    } else {
+      const int rs = j % C::kTileRing;
+      if (!wait0(ring.empty(rs), ((j / C::kTileRing) & 1u) ^ 1u, 9)) break;
+      if (lead) {
+        w = fetch_tile<C::kTileRing>(p, j);
+        ring.slots[rs] = w;
+        ptx::mbar_arrive(ring.full(rs));
+      }
+      w = __shfl_sync(lanes, w, 0);
+      if (w < 0) break;
     }
-    w = __shfl_sync(lanes, w, 0);
-    if (w < 0) break;
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
     if (ti.n_kv == 0) continue;
+    if (MODE != 2) {
 #pragma unroll
-    for (int t = 0; t < C::QT; ++t) {
-      if (!wait0(bar(C::kBarQEmpty + t), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
-      if (lead) {
-        ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
-        load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
-                  bar(C::kBarQFull + t));
+      for (int t = 0; t < C::QT; ++t) {
+        if (!wait0(bar(C::kBarQEmpty + t), (tcount & 1u) ^ 1u, 1)) { ok = false; break; }
+        if (lead) {
+          ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+          load_tile(tq, ti.h, ti.qtok + ti.q0 + 128 * t, sbase + C::kOffQ + t * C::kTileBytes,
+                    bar(C::kBarQFull + t));
+        }
       }
+      if (!ok) break;
+      ++tcount;
     }
-    if (!ok) break;
-    ++tcount;
     const int n = ti.n_kv;
     const int kb0 = ti.kb0;   // first key block of the tile's range
     if (C::QT == 2) {
       // consumption order of the MMA warp: K0, V0, K1, V1, ...
       for (int i = 0; ok && i < n; ++i) {
-        ok = load_kv(tk, ti, kb0 + i) && load_kv(tv, ti, kb0 + i);
+        ok = load_kv(tk, ti, kb0 + i, do_k) && load_kv(tv, ti, kb0 + i, do_v);
       }
     } else {
       // consumption order: K0, K1, V0, K2, V1, ..., V_{n-1}
-      ok = load_kv(tk, ti, kb0);
+      ok = load_kv(tk, ti, kb0, do_k);
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n) ok = load_kv(tk, ti, kb0 + i + 1);
-        if (ok) ok = load_kv(tv, ti, kb0 + i);
+        if (i + 1 < n) ok = load_kv(tk, ti, kb0 + i + 1, do_k);
+        if (ok) ok = load_kv(tv, ti, kb0 + i, do_v);
       }
     }
   }
   if (lead && *wt.abort_flag) {
     // let the copies still in flight land before the CTA's memory goes away
+    // (each paged warp drains the slots it filled itself)
     const uint32_t first = kvc > (uint32_t)C::STAGES ? kvc - C::STAGES : 0u;
     for (uint32_t c = first; c < kvc; ++c)
-      wt.drain(bar(C::kBarKVFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u);
-    for (int t = 0; t < C::QT && tcount > 0; ++t) wt.drain(bar(C::kBarQFull + t), (tcount - 1) & 1u);
+      if ((acted >> (kvc - 1u - c)) & 1u) wt.drain(bar(C::kBarKVFull + (int)(c % C::STAGES)), (c / C::STAGES) & 1u);
+    if (MODE != 2)
+      for (int t = 0; t < C::QT && tcount > 0; ++t) wt.drain(bar(C::kBarQFull + t), (tcount - 1) & 1u);
   }
 }
 
@@ -687,7 +714,7 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int e = 64 * hf + 4 * j;
-            pk[j] = ptx::pack_e4m3x2(s[e], s[e + 1]) | (ptx::pack_e4m3x2(s[e + 2], s[e + 3]) << 16);
+            pk[j] = ptx::pack_e4m3x4(s[e], s[e + 1], s[e + 2], s[e + 3]);
           }
           ptx::tmem_st16(s_addr + 16 * hf, pk);
         } else {
@@ -785,7 +812,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
       if (i >= C::kBarPFull && i < C::kBarPFull + 4) count = 4;
-      if (i >= C::kBarTileEmpty) count = C::kTileConsumers;
+      if (i >= C::kBarTileEmpty) count = C::kTileConsumers + (p.block_table != nullptr ? 1 : 0);
       ptx::mbar_init(bars + 8u * i, count);
     }
     *abort_flag = 0;
@@ -812,7 +839,12 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kRebalance) ptx::setmaxnreg_dec<C::kRegsLow>();
     if (warp == C::kLoadWarp) {
-      if (p.block_table != nullptr || lane == 0) load_role<C, CAUSAL>(&tq, &tk, &tv, p, sbase, wt, ring);
+      if (p.block_table != nullptr)
+        load_role<C, CAUSAL, 1>(&tq, &tk, &tv, p, sbase, wt, ring);
+      else if (lane == 0)
+        load_role<C, CAUSAL, 0>(&tq, &tk, &tv, p, sbase, wt, ring);
+    } else if (warp == C::kVLoadWarp) {
+      if (p.block_table != nullptr) load_role<C, CAUSAL, 2>(&tq, &tk, &tv, p, sbase, wt, ring);
     } else if (warp == C::kMmaWarp) {
       if (lane == 0) mma_role<C, CAUSAL>(p, sbase, tmem, wt, ring);
     }

@@ -279,10 +279,17 @@ __device__ __forceinline__ void exp2_poly2(float& a, float& b, float c0, float c
   b = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
 }
 
-// two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448), lo in the low byte
-__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// four fp32 -> four e4m3 codes (round to nearest even, saturate to +-448) in
+// one word, a in the low byte: both pair conversions write 16-bit halves that
+// are joined without a shift or an or
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
   return r;
 }
 __device__ __forceinline__ float ex2(float x) {

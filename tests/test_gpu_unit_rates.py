@@ -31,3 +31,28 @@ def test_unit_rates(cuda_device, tmp_path):
         print(f"{name:40s} {rates[name]:8.2f} instructions / clock / SM")
     for r in rates.values():
         assert 1.0 <= r <= 1024.0
+
+
+def test_tma_small_box_issue(cuda_device, tmp_path):
+    """Small TMA boxes (16 rows x 128 bytes, the paged K/V box at 16-key pages)
+    from one warp against several warps with the same bytes in flight. Prints
+    GB/s per configuration; asserts only that every run finished."""
+    so = str(tmp_path / "tma_issue.so")
+    subprocess.run([fa_build.nvcc(), *fa_build.ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                    "-cudart", "shared", os.path.join(HERE, "gpu_helpers", "tma_issue.cu"), "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    lib.tma_issue_rate.restype = ctypes.c_double
+    lib.tma_issue_rate.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    rows = 262144                                  # [rows, 2048] bf16 = 1 GiB, rows of 4 KB
+    buf = torch.zeros(rows * 2048, dtype=torch.bfloat16, device=cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for box_rows, warps, ops in [(16, 1, 16), (16, 1, 32), (16, 2, 16), (16, 4, 8), (64, 1, 8), (128, 1, 4)]:
+        per_batch = sms * warps * ops * box_rows * 128
+        batches = max(4, (4 << 30) // per_batch)
+        gbs = lib.tma_issue_rate(buf.data_ptr(), rows, box_rows, warps, ops, batches, sms, err.data_ptr())
+        torch.cuda.synchronize()
+        print(f"box {box_rows:3d} rows x 128 B, {warps} warp(s) x {ops:2d} boxes in flight "
+              f"({warps * ops * box_rows * 128 // 1024:3d} KB per SM): {gbs:8.1f} GB/s")
+        assert gbs > 0.0, gbs
+    assert int(err.item()) == 0
