@@ -56,3 +56,28 @@ def test_tma_small_box_issue(cuda_device, tmp_path):
               f"({warps * ops * box_rows * 128 // 1024:3d} KB per SM): {gbs:8.1f} GB/s")
         assert gbs > 0.0, gbs
     assert int(err.item()) == 0
+
+
+def test_mma_issue_rate(cuda_device, tmp_path):
+    """Back-to-back tcgen05.mma M128 N128 K16 (bf16) from one thread per SM,
+    descriptors built as in the forward kernel: cycles per product for the
+    QK^T form (both operands in shared memory) and the PV form (A in tensor
+    memory, B MN-major). Nominal: 64 cycles (8192 dense bf16 FLOP per clock
+    per SM). Prints; asserts only that the runs finished."""
+    so = str(tmp_path / "mma_issue.so")
+    csrc = os.path.join(os.path.dirname(HERE), "exact_attention_forward_tiled_gb300", "csrc")
+    subprocess.run([fa_build.nvcc(), *fa_build.ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                    "-cudart", "shared", "-I", csrc, os.path.join(HERE, "gpu_helpers", "mma_issue.cu"), "-o", so],
+                   check=True)
+    lib = ctypes.CDLL(so)
+    lib.mma_issue_cycles.restype = ctypes.c_double
+    lib.mma_issue_cycles.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device=cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for form, name in ((0, "QK^T form (SS, B K-major)"), (1, "PV form (A in tensor memory, B MN-major)")):
+        lib.mma_issue_cycles(form, 16, sms, cyc.data_ptr(), err.data_ptr())
+        c = lib.mma_issue_cycles(form, 2048, sms, cyc.data_ptr(), err.data_ptr())
+        print(f"{name:42s} {c:6.1f} cycles per M128 N128 K16 product ({64.0 / c * 100:5.1f} % of nominal)")
+        assert c > 0.0, c
+    assert int(err.item()) == 0
