@@ -33,9 +33,20 @@ Parity status of each function (what pins it; see tests/test_oracle_*.py):
   to zero, dV rows sum to the dO rows, linearity in dO).
 * ``attention_backward_sampled`` -- pinned: equals ``attention_backward_head``
   at every row on small inputs.
-* ``block_scales`` / ``fp8_attention_emulated`` -- parity unpinned beyond the
-  special cases in the tests: the block granularity, the amax/448 scale and
-  the rule that quantises P are readings of pages that leave them open.
+* ``attention_rows`` -- pinned: equals ``attention`` at the same rows, bit for
+  bit (and shares its C core, which the mutant tests cover).
+* ``merge_partials`` -- pinned: attention over disjoint key ranges, merged,
+  equals attention over all keys from the definition; empty ranges merge to
+  the other range (O = 0, LSE = -inf when every range is empty).
+* ``visible_pairs`` -- pinned: brute-force counts of tiny causal and
+  non-causal cases.
+* ``e4m3_round`` -- decode of encode, both pinned above.
+* ``quantize_blocks`` -- pinned: idempotent, and every value within the e4m3
+  half-ulp bound (2^-4 relative) of its input.
+* ``block_scales`` / ``tensor_scale`` / ``fp8_attention_emulated`` -- parity
+  unpinned beyond the special cases in the tests: the block granularity, the
+  amax/448 scale and the rule that quantises P are readings of pages that
+  leave them open.
 """
 from __future__ import annotations
 
