@@ -472,7 +472,7 @@ def main(argv=None):
                                             w.D, stream=st),
                     lambda: api.fp8_attention_forward(prep, causal=w.causal, scale=scale, out=o_[0], lse=o_[1],
                                                       stream=st)]
-        names = ["fp8_prep_rows_kernel", "fa_fwd_kernel"]
+        names = ["fp8_prep_kernel", "fa_fwd_kernel"]
     elif w.splitkv:
         ws_bytes = api.fa_fwd_splitkv_workspace_size(w.B, w.H, Sq, Sk, w.D, 0)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -643,9 +643,9 @@ def main(argv=None):
         pb = A.prep_bytes(w.H, w.D, w.B, w.Sq)
         gbs = pb / (per_kernel[0] * 1e-3) / 1e9
         line["prep_roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                 "frac": gbs / peaks["hbm_gbs"], "kernel": "fp8_prep_rows_kernel",
+                                 "frac": gbs / peaks["hbm_gbs"], "kernel": "fp8_prep_kernel",
                                  "kernel_ms": per_kernel[0], "bytes": pb,
-                                 "traffic": committed_traffic("fp8_prep_rows_kernel", w.name)}
+                                 "traffic": committed_traffic("fp8_prep_kernel", w.name)}
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         host = {"q": q.cpu(), "k": k.cpu(), "v": v.cpu(), "cu_seqlens_q": inputs["cu_seqlens_q"]}
         if w.backward:

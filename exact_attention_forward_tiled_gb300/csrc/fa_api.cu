@@ -473,25 +473,19 @@ int prep_impl(const void* q, const void* k, const void* v, int in_dtype, void* q
     add(k, k8, k_scale, sigma, Sk, cu_k, cbk, total_k);
     add(v, v8, v_scale, nullptr, Sk, cu_k, cbk, total_k);
   }
-  // one [rows, H * D] map per tensor. D <= 128: the input in 64-element boxes
-  // with the 128-byte swizzle (a thread reads its row across the banks) and
-  // the e4m3 output in one D-byte x 128-row box; D = 256: one unswizzled box
-  // of a 128-row block of one head (read row by row from shared memory)
+  // one [rows, H * D] map per tensor: the input in 64-element boxes with the
+  // 128-byte swizzle (a thread reads its row across the banks), the e4m3
+  // output in boxes of min(D, 128) bytes x 128 rows (64- or 128-byte swizzle)
   CUtensorMap in_maps[3], out_maps[3];
   const CUtensorMapDataType dt = in_dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int i = 0; i < n; ++i) {
     const uint64_t rows = t[i].cu_seqlens != nullptr ? (uint64_t)t[i].total : (uint64_t)t[i].B * t[i].S;
     const uint64_t cols = (uint64_t)H * D;
-    if (D <= 128) {
-      if ((st = make_map(&in_maps[i], t[i].x, dt, 2, cols, rows, 64, 128)) != FA_OK) return st;
-      if ((st = make_map(&out_maps[i], t[i].x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cols, rows, (uint32_t)D, 128,
-                         D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) != FA_OK)
-        return st;
-    } else if ((st = make_map(&in_maps[i], t[i].x, dt, 2, cols, rows, (uint32_t)D, 128,
-                              CU_TENSOR_MAP_SWIZZLE_NONE)) != FA_OK) {
+    if ((st = make_map(&in_maps[i], t[i].x, dt, 2, cols, rows, 64, 128)) != FA_OK) return st;
+    if ((st = make_map(&out_maps[i], t[i].x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cols, rows, D == 64 ? 64u : 128u,
+                       128, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
       return st;
-    }
   }
   cudaError_t e = fa::launch_fp8_prep(t, in_maps, out_maps, n, D, dev->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {

@@ -169,10 +169,10 @@ struct PrepParams {
   int* status;            // device status word (bad cu_seqlens entries)
 };
 cudaError_t launch_varlen_blocks(const int* cu_seqlens, int B, int* cu_blocks, cudaStream_t stream);
-// in_maps: [rows, H * D] tensor maps of the 16-bit inputs; D <= 128: boxes of
-// 64 elements x 128 rows with the 128-byte swizzle, D = 256: one unswizzled
-// D x 128 box. out_maps (D <= 128): [rows, H * D] maps of the e4m3 outputs,
-// one D x 128 box, 128-byte swizzle for D = 128, 64-byte for D = 64.
+// in_maps: [rows, H * D] tensor maps of the 16-bit inputs, boxes of 64
+// elements x 128 rows with the 128-byte swizzle. out_maps: [rows, H * D] maps
+// of the e4m3 outputs, boxes of min(D, 128) bytes x 128 rows, 64-byte swizzle
+// for D = 64, 128-byte otherwise.
 cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* in_maps, const CUtensorMap* out_maps,
                             int n_tensors, int D, int num_sms, cudaStream_t stream);
 

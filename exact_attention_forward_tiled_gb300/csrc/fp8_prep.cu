@@ -9,10 +9,10 @@
 // TMA copy brings the next block into shared memory while the current one is
 // rotated in registers, its amax is reduced through shared memory and its
 // codes are written, so every element is read from HBM once and written once,
-// with reads in flight throughout. For D <= 128 a thread owns a whole row and
-// runs its Walsh-Hadamard transform on packed fp32 pairs without any
-// cross-lane traffic (fp8_prep_rows_kernel); D = 256 spreads a row over 32
-// lanes and finishes the transform with shuffles (fp8_prep_lanes_kernel).
+// with reads in flight throughout. A thread owns a whole row (D <= 128) or
+// half of one (D = 256) and runs the Walsh-Hadamard transform on packed fp32
+// pairs in its registers; at D = 256 the last butterfly crosses to the
+// neighbouring lane.
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -28,23 +28,9 @@ struct PrepBatch {
   int n;
 };
 
-// Eight consecutive 16-bit elements (16 bytes, read from shared memory) -> fp32.
-__device__ __forceinline__ void cvt8(uint4 u, bool bf16, float (&x)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint16_t lo = w[k] & 0xffffu, hi = w[k] >> 16;
-    x[2 * k] = bf16 ? __uint_as_float((uint32_t)lo << 16) : __half2float(__ushort_as_half(lo));
-    x[2 * k + 1] = bf16 ? __uint_as_float((uint32_t)hi << 16) : __half2float(__ushort_as_half(hi));
-  }
-}
-
 struct PrepMaps {
   CUtensorMap m[3];
 };
-
-// shared-memory block buffers per CTA (NB - 1 blocks fetched ahead)
-constexpr int kPrepBuffers = 2;
 
 // Where block `bid` (counted over all tensors of the batch) lives: tensor,
 // head, first token, valid rows, scale index; false if the block starts past
@@ -88,163 +74,6 @@ __device__ __forceinline__ bool prep_block(const PrepBatch& pb, int bid, PrepBlo
   return true;
 }
 
-// D = 256. Persistent CTAs, each walking blocks bid = blockIdx.x, + gridDim.x, ...
-// A block is 128 rows x D of one head of one tensor. Thread 0 fetches the
-// next block with one TMA copy into the other half of a shared-memory double
-// buffer while the CTA works on the current one, so HBM reads stay in flight
-// while the CTA rotates, reduces and stores.
-//
-// The work on a block: a row is spread over LPR = D/8 lanes holding 8
-// consecutive elements each; the Walsh-Hadamard transform runs in registers
-// (butterflies over the bits of d inside a lane, then across lanes with
-// shuffles), the block amax is reduced through shared memory, and the codes
-// are written with 8-byte stores.
-template <int D>
-__global__ void __launch_bounds__(32 * (D == 256 ? 32 : 16), D == 256 ? 1 : 2)
-    fp8_prep_lanes_kernel(const __grid_constant__ PrepMaps maps, const PrepBatch pb, int total_blocks) {
-  constexpr int NW = D == 256 ? 32 : 16;  // warps per CTA
-  constexpr int LPR = D / 8;               // lanes per row
-  constexpr int RPI = 32 / LPR;            // rows per warp instruction
-  constexpr int RPW = 128 / NW;            // rows per warp
-  constexpr int ITER = RPW / RPI;
-  constexpr int LOG_D = D == 64 ? 6 : (D == 128 ? 7 : 8);
-  constexpr uint32_t kBlockBytes = 128u * D * 2u;
-  constexpr int NB = kPrepBuffers;
-  extern __shared__ __align__(128) uint8_t prep_smem[];
-  __shared__ float red[NW];
-  __shared__ __align__(8) uint64_t full_bar[NB];
-  __shared__ int gave_up;
-  const uint32_t buf0 = ptx::smem_u32(prep_smem);
-  const uint32_t bar0 = ptx::smem_u32(&full_bar[0]);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / LPR;              // row of the instruction this lane serves
-  const int d0 = (lane % LPR) * 8;         // first element of the lane
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) ptx::mbar_init(bar0 + 8u * i, 1);
-    ptx::fence_mbar_init();
-    gave_up = 0;
-  }
-  __syncthreads();
-
-  // thread 0: fetch block `bid` into buffer `s` (nothing if it is skipped)
-  auto fetch = [&](int bid, int s) {
-    PrepBlock pbk;
-    if (bid < total_blocks && prep_block(pb, bid, pbk)) {
-      ptx::mbar_arrive_expect_tx(bar0 + 8u * s, kBlockBytes);
-      ptx::tma_load_2d(buf0 + s * kBlockBytes, &maps.m[pbk.ti], pbk.h * D, (int)(pbk.start + pbk.blk * 128),
-                       bar0 + 8u * s);
-    }
-  };
-  // NB - 1 blocks ahead
-  if (threadIdx.x == 0)
-    for (int i = 0; i < NB - 1; ++i) fetch(blockIdx.x + i * gridDim.x, i);
-  uint32_t phase_bits = 0u;   // bit i: parity of buffer i's next completion
-
-  int s = 0;
-  for (int bid = blockIdx.x; bid < total_blocks; bid += gridDim.x, s = (s + 1) % NB) {
-    PrepBlock pbk;
-    const bool live = prep_block(pb, bid, pbk);
-    // block bid + (NB - 1) * gridDim.x goes into the buffer the previous
-    // iteration used, free since the __syncthreads that ended it
-    if (threadIdx.x == 0) fetch(bid + (NB - 1) * gridDim.x, (s + NB - 1) % NB);
-    if (!live) continue;
-    const PrepParams& P = pb.t[pbk.ti];
-    // bounded wait for this block's copy: thread 0 waits, the CTA learns the
-    // outcome at the barrier (the barrier also publishes the copied data)
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar0 + 8u * s, (phase_bits >> s) & 1u)) {
-        if (ptx::globaltimer_ns() - t0 > 2000000000ull) {
-          atomicOr(P.status, kDevTimeout | 0x40);
-          gave_up = 1;
-          break;
-        }
-      }
-    }
-    phase_bits ^= 1u << s;
-    __syncthreads();
-    if (gave_up) return;
-    const uint8_t* blkmem = prep_smem + s * kBlockBytes;
-
-    float sg[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sg[j] = P.sigma ? (float)P.sigma[d0 + j] : 1.f;
-    // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
-    const float norm = P.sigma ? rsqrtf((float)D) : 1.f;
-
-    float x[ITER][8];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < ITER; ++i) {
-      const int row = warp * RPW + i * RPI + sub;   // within the block
-      if (pbk.blk * 128 + row < pbk.L) {
-        cvt8(*reinterpret_cast<const uint4*>(blkmem + (row * D + d0) * 2), P.bf16, x[i]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < ITER; ++i) {
-      if (P.sigma) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] *= sg[j];
-        // Walsh-Hadamard butterflies over the three bits of d inside the lane
-#pragma unroll
-        for (int bit = 0; bit < 3; ++bit) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (j & (1 << bit)) continue;
-            const float a = x[i][j], c = x[i][j | (1 << bit)];
-            x[i][j] = a + c;
-            x[i][j | (1 << bit)] = a - c;
-          }
-        }
-        // ... and over the bits of d that select the lane (within the row's
-        // lanes): lower partner a + b, upper partner a - b = other - mine, one
-        // FFMA each with the sign of the lane's half
-#pragma unroll
-        for (int bit = 3; bit < LOG_D; ++bit) {
-          const int m = 1 << (bit - 3);
-          const float sgn = (lane & m) ? -1.f : 1.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, x[i][j], m);
-            x[i][j] = fmaf(x[i][j], sgn, other);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-    if (lane == 0) red[warp] = amax;
-    __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
-    amax *= norm;   // amax of the rotated, normalised values
-    const float scale = amax > 0.f ? amax / 448.f : 1.f;
-    const float inv = norm / scale;
-    if (threadIdx.x == 0) P.scale[pbk.sidx] = scale;
-
-#pragma unroll
-    for (int i = 0; i < ITER; ++i) {
-      const int row = pbk.blk * 128 + warp * RPW + i * RPI + sub;
-      if (row >= pbk.L) continue;
-      *reinterpret_cast<uint2*>(P.x8 + ((pbk.start + row) * P.H + pbk.h) * D + d0) =
-          make_uint2(ptx::pack_e4m3x4(x[i][0] * inv, x[i][1] * inv, x[i][2] * inv, x[i][3] * inv),
-                     ptx::pack_e4m3x4(x[i][4] * inv, x[i][5] * inv, x[i][6] * inv, x[i][7] * inv));
-    }
-    // red[] and this buffer are reused by the next iterations
-    __syncthreads();
-  }
-}
-
-// ------------------------------------------------------------ D <= 128
 // Two 16-bit elements -> fp32 (bf16: the bits shifted into place; fp16: the
 // hardware conversion).
 template <bool BF16>
@@ -267,22 +96,27 @@ __device__ __forceinline__ uint32_t swizzled(uint32_t o) {
   return o ^ (((o >> 7) & (SW == 128 ? 7u : 3u)) << 4);
 }
 
-// Row r of a 128 x D block (D / 64 input boxes of 64 elements x 128 rows,
-// 128-byte swizzle) into v: v[i] holds elements 2i and 2i + 1. With ROT the
-// row gets its sign flips (XOR of the sign bits, bit 15 of each 16-bit
-// element, by mask) and the whole D-point Walsh-Hadamard transform: the
-// butterfly over bit 0 of d pairs the two halves of a packed register, every
-// other bit pairs two registers, so all but the first stage are f32x2 adds and
-// subtracts. Returns max |x| over the row.
-template <int D, bool ROT, bool BF16>
-__device__ __forceinline__ float load_row(const uint8_t* blk, int r, const uint32_t* mask, uint64_t (&v)[D / 2]) {
-  constexpr int NP = D / 2;
+// E elements of row r of a 128 x D block (D / 64 input boxes of 64 elements
+// x 128 rows, 128-byte swizzle), starting at element e0 (0, or 128 for the
+// second half of a D = 256 row), into v: v[i] holds elements e0 + 2i and
+// e0 + 2i + 1. With ROT the elements get their sign flips (XOR of the sign
+// bits, bit 15 of each 16-bit element, by mask) and the E-point
+// Walsh-Hadamard transform: the butterfly over bit 0 of d pairs the two
+// halves of a packed register, every other bit pairs two registers, so all but
+// the first stage are f32x2 adds and subtracts. Returns max |x| over the E
+// elements (before any stage that crosses to another thread).
+template <int E, bool ROT, bool BF16>
+__device__ __forceinline__ float load_row(const uint8_t* blk, int r, int e0, const uint32_t* mask,
+                                          uint64_t (&v)[E / 2]) {
+  constexpr int NP = E / 2;
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
-    const uint32_t off = (uint32_t)(c / 8) * 16384u + swizzled<128>((uint32_t)r * 128u + (uint32_t)(c % 8) * 16u);
+  for (int c = 0; c < E / 8; ++c) {
+    const int e = e0 + 8 * c;
+    const uint32_t off =
+        (uint32_t)(e / 64) * 16384u + swizzled<128>((uint32_t)r * 128u + (uint32_t)((e % 64) / 8) * 16u);
     uint4 u = *reinterpret_cast<const uint4*>(blk + off);
     if (ROT) {
-      const uint4 m = *reinterpret_cast<const uint4*>(mask + 4 * c);
+      const uint4 m = *reinterpret_cast<const uint4*>(mask + e / 2);
       u.x ^= m.x;
       u.y ^= m.y;
       u.z ^= m.z;
@@ -318,35 +152,50 @@ __device__ __forceinline__ float load_row(const uint8_t* blk, int r, const uint3
   return amax;
 }
 
-// D = 64, 128. Persistent CTAs of 128 threads walk the blocks; thread r owns
-// row r of the current block. Thread 0 keeps the next block's TMA copy in
-// flight (two shared-memory buffers) while the CTA rotates the current one in
-// registers; the block amax goes through one CTA barrier; the codes of a full
-// block are written back into its buffer (its input has been read by then)
-// and leave with one TMA store, those of a ragged last block with plain
-// stores of the valid rows.
+// Persistent CTAs walk the blocks; each row of the current block belongs to
+// TPR threads (1, or 2 at D = 256), each of which owns E = D / TPR elements of
+// it. Thread 0 keeps the next block's TMA copy in flight (two shared-memory
+// buffers) while the CTA rotates the current one in registers; the block amax
+// goes through one CTA barrier; the codes of a full block are written back
+// into its buffer (its input has been read by then) and leave with TMA stores,
+// those of a ragged last block with plain stores of the valid rows.
 template <int D>
-__global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
-    fp8_prep_rows_kernel(const __grid_constant__ PrepMaps in_maps, const __grid_constant__ PrepMaps out_maps,
-                         const PrepBatch pb, int total_blocks) {
-  constexpr int NP = D / 2;
-  constexpr uint32_t kBlockBytes = 128u * D * 2u;
-  constexpr int kOutSwizzle = D == 128 ? 128 : 64;   // the output map's swizzle (rows of D bytes)
+struct PrepCfg {
+  static constexpr int TPR = D == 256 ? 2 : 1;           // threads per row
+  static constexpr int E = D / TPR;                        // elements per thread
+  static constexpr int kThreads = 128 * TPR;
+  static constexpr int kCtasPerSm = D == 64 ? 5 : (D == 128 ? 3 : 1);
+  static constexpr uint32_t kBlockBytes = 128u * D * 2u;   // one 16-bit input block
+  static constexpr int kOutBox = D == 64 ? 64 : 128;       // bytes per row of an output box
+  static constexpr int kOutSwizzle = kOutBox;              // that box's swizzle (64 or 128 bytes)
+  static constexpr size_t kSmemBytes = 2u * kBlockBytes + 1024u;
+};
+
+template <int D>
+__global__ void __launch_bounds__(PrepCfg<D>::kThreads, PrepCfg<D>::kCtasPerSm)
+    fp8_prep_kernel(const __grid_constant__ PrepMaps in_maps, const __grid_constant__ PrepMaps out_maps,
+                    const PrepBatch pb, int total_blocks) {
+  using C = PrepCfg<D>;
+  constexpr int E = C::E, NP = E / 2, NW = C::kThreads / 32;
+  constexpr uint32_t kBlockBytes = C::kBlockBytes;
   extern __shared__ uint8_t prep_raw[];
-  __shared__ float red[4];
+  __shared__ float red[NW];
   __shared__ __align__(8) uint64_t full_bar[2];
-  __shared__ __align__(16) uint32_t smask[3][NP];
+  __shared__ __align__(16) uint32_t smask[3][D / 2];
   __shared__ int gave_up;
   // 1024-byte aligned buffers (the swizzle pattern repeats every 1024 bytes)
   const uint32_t raw = ptx::smem_u32(prep_raw);
   const uint32_t buf0 = (raw + 1023u) & ~1023u;
   uint8_t* const buf0_ptr = prep_raw + (buf0 - raw);
   const uint32_t bar0 = ptx::smem_u32(&full_bar[0]);
-  const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = threadIdx.x / C::TPR;        // row of the block
+  const int half = threadIdx.x % C::TPR;     // which E elements of it (partner: the next lane)
+  const int e0 = half * E;
 
   // sign masks of each tensor's sigma (+-1), two elements per word
-  for (int i = threadIdx.x; i < 3 * NP; i += blockDim.x) {
-    const int ti = i / NP, j = i % NP;
+  for (int i = threadIdx.x; i < 3 * (D / 2); i += blockDim.x) {
+    const int ti = i / (D / 2), j = i % (D / 2);
     const int8_t* sg = ti < pb.n ? pb.t[ti].sigma : nullptr;
     smask[ti][j] = sg != nullptr ? (sg[2 * j] < 0 ? 0x8000u : 0u) | (sg[2 * j + 1] < 0 ? 0x80000000u : 0u) : 0u;
   }
@@ -380,7 +229,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
     PrepBlock pbk;
     const bool live = prep_block(pb, bid, pbk);
     if (threadIdx.x == 0) {
-      // the other buffer last held the previous block's codes: its store
+      // the other buffer last held the previous block's codes: its stores
       // must have read them before the next block is copied in
       ptx::bulk_wait_read_all();
       if (fetch(bid + gridDim.x, s ^ 1)) pending |= 1u << (s ^ 1);
@@ -394,18 +243,34 @@ __global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
     pending &= ~(1u << s);
     const int valid = min(128, pbk.L - pbk.blk * 128);
     uint8_t* const blk = buf0_ptr + s * kBlockBytes;
+    const bool rot = P.sigma != nullptr;
 
     uint64_t v[NP];
     float amax = 0.f;
     if (ok && r < valid) {
       const uint32_t* m = smask[pbk.ti];
-      if (P.sigma != nullptr)
-        amax = P.bf16 ? load_row<D, true, true>(blk, r, m, v) : load_row<D, true, false>(blk, r, m, v);
+      if (rot)
+        amax = P.bf16 ? load_row<E, true, true>(blk, r, e0, m, v) : load_row<E, true, false>(blk, r, e0, m, v);
       else
-        amax = P.bf16 ? load_row<D, false, true>(blk, r, m, v) : load_row<D, false, false>(blk, r, m, v);
+        amax = P.bf16 ? load_row<E, false, true>(blk, r, e0, m, v) : load_row<E, false, false>(blk, r, e0, m, v);
     } else {
 #pragma unroll
       for (int i = 0; i < NP; ++i) v[i] = 0ull;
+    }
+    if (C::TPR == 2 && rot) {
+      // butterfly over bit 7 of d: the lower half becomes mine + other, the
+      // upper half other - mine (one FMA each with the sign of the half);
+      // both lanes of a row take the same branch (rot is per block)
+      const uint64_t sgn = half ? ptx::f2pack(-1.f, -1.f) : ptx::f2pack(1.f, 1.f);
+      amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+        v[i] = ptx::fma2(v[i], sgn, other);
+        float a, b;
+        ptx::f2unpack(v[i], a, b);
+        amax = ptx::max3(amax, fabsf(a), fabsf(b));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -421,8 +286,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
       return;
     }
     // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
-    const float norm = P.sigma != nullptr ? rsqrtf((float)D) : 1.f;
-    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) * norm;
+    const float norm = rot ? rsqrtf((float)D) : 1.f;
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < NW; ++i) amax = fmaxf(amax, red[i]);
+    amax *= norm;
     const float scale = amax > 0.f ? amax / 448.f : 1.f;
     const float inv = norm / scale;
     if (threadIdx.x == 0) P.scale[pbk.sidx] = scale;
@@ -438,20 +306,28 @@ __global__ void __launch_bounds__(128, D == 64 ? 5 : 3)
     }
     const int row0 = pbk.blk * 128;
     if (valid == 128) {
+      // codes in the output boxes' layout (D / kOutBox boxes of kOutBox-byte
+      // rows, each box 128 rows), then one TMA store per box
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c)
-        *reinterpret_cast<uint4*>(blk + swizzled<kOutSwizzle>((uint32_t)r * D + (uint32_t)c * 16u)) =
-            make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+      for (int c = 0; c < E / 16; ++c) {
+        const int e = e0 + 16 * c;
+        const uint32_t off = (uint32_t)(e / C::kOutBox) * (128u * C::kOutBox) +
+                             swizzled<C::kOutSwizzle>((uint32_t)r * C::kOutBox + (uint32_t)(e % C::kOutBox));
+        *reinterpret_cast<uint4*>(blk + off) = make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+      }
       ptx::fence_proxy_async_smem();
       __syncthreads();
       if (threadIdx.x == 0) {
-        ptx::tma_store_2d(&out_maps.m[pbk.ti], buf0 + s * kBlockBytes, pbk.h * D, (int)(pbk.start + row0));
+#pragma unroll
+        for (int b = 0; b < D / C::kOutBox; ++b)
+          ptx::tma_store_2d(&out_maps.m[pbk.ti], buf0 + s * kBlockBytes + b * (128u * C::kOutBox),
+                            pbk.h * D + b * C::kOutBox, (int)(pbk.start + row0));
         ptx::bulk_commit();
       }
     } else if (r < valid) {
-      uint8_t* dst = P.x8 + ((pbk.start + row0 + r) * P.H + pbk.h) * D;
+      uint8_t* dst = P.x8 + ((pbk.start + row0 + r) * P.H + pbk.h) * D + e0;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c)
+      for (int c = 0; c < E / 16; ++c)
         *reinterpret_cast<uint4*>(dst + 16 * c) =
             make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
     }
@@ -486,34 +362,33 @@ cudaError_t launch_fp8_prep(const PrepParams* tensors, const CUtensorMap* in_map
   for (int i = 0; i < n_tensors; ++i) {
     pb.t[i] = tensors[i];
     pin.m[i] = in_maps[i];
-    if (D <= 128) pout.m[i] = out_maps[i];
+    pout.m[i] = out_maps[i];
     pb.count[i] = tensors[i].B * tensors[i].H * tensors[i].nblk;
     total += pb.count[i];
   }
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffL) return cudaErrorInvalidValue;
+  // resident CTAs per SM: shared memory (two 128 x D blocks of 16-bit
+  // elements + alignment) and registers (E fp32 per thread)
+  auto run = [&](auto kern, int threads, int per_sm, size_t smem) -> cudaError_t {
+    const int grid = (int)(total < (long)per_sm * num_sms ? total : (long)per_sm * num_sms);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) kern<<<grid, threads, smem, stream>>>(pin, pout, pb, (int)total);
+    return e;
+  };
   cudaError_t e;
-  if (D == 64 || D == 128) {
-    // resident CTAs per SM: shared memory (two blocks of 128 x D 16-bit
-    // elements + alignment) and registers (a row of D fp32 per thread)
-    const long per_sm = D == 64 ? 5L : 3L;
-    const int grid = (int)(total < per_sm * num_sms ? total : per_sm * num_sms);
-    const size_t smem = 2u * 128u * (size_t)D * 2u + 1024u;
-    if (D == 64) {
-      e = cudaFuncSetAttribute(fp8_prep_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) fp8_prep_rows_kernel<64><<<grid, 128, smem, stream>>>(pin, pout, pb, (int)total);
-    } else {
-      e = cudaFuncSetAttribute(fp8_prep_rows_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) fp8_prep_rows_kernel<128><<<grid, 128, smem, stream>>>(pin, pout, pb, (int)total);
-    }
-  } else if (D == 256) {
-    // one resident CTA per SM (1024 threads, kPrepBuffers 128 x 256 blocks)
-    const int grid = (int)(total < num_sms ? total : num_sms);
-    const size_t smem = (size_t)kPrepBuffers * 128u * (size_t)D * 2u;
-    e = cudaFuncSetAttribute(fp8_prep_lanes_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) fp8_prep_lanes_kernel<256><<<grid, 32 * 32, smem, stream>>>(pin, pb, (int)total);
-  } else {
-    return cudaErrorInvalidValue;
+  switch (D) {
+    case 64:
+      e = run(fp8_prep_kernel<64>, PrepCfg<64>::kThreads, PrepCfg<64>::kCtasPerSm, PrepCfg<64>::kSmemBytes);
+      break;
+    case 128:
+      e = run(fp8_prep_kernel<128>, PrepCfg<128>::kThreads, PrepCfg<128>::kCtasPerSm, PrepCfg<128>::kSmemBytes);
+      break;
+    case 256:
+      e = run(fp8_prep_kernel<256>, PrepCfg<256>::kThreads, PrepCfg<256>::kCtasPerSm, PrepCfg<256>::kSmemBytes);
+      break;
+    default:
+      return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
