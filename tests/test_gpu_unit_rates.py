@@ -81,3 +81,37 @@ def test_mma_issue_rate(cuda_device, tmp_path):
         print(f"{name:42s} {c:6.1f} cycles per M128 N128 K16 product ({64.0 / c * 100:5.1f} % of nominal)")
         assert c > 0.0, c
     assert int(err.item()) == 0
+
+
+def test_fp8_prep_rates(cuda_device):
+    """fa_fp8_prep throughput at D = 64 / 128 / 256 with the same bytes (bf16
+    Q, K, V of 4 x 8192 tokens, H = 32 / 16 / 8): GB/s of the algorithmic
+    bytes (3 per element: 2 read, 1 written), CUDA events around 50 calls.
+    Prints; asserts only that the calls ran."""
+    from exact_attention_forward_tiled_gb300 import api
+    from exact_attention_forward_tiled_gb300 import build as fa_build_mod
+    fa_build_mod.build()
+    g = torch.Generator(device=cuda_device).manual_seed(0)
+    for H, D in ((32, 64), (16, 128), (8, 256)):
+        B, S = 4, 8192
+        q, k, v = (torch.randn((B * S, H, D), generator=g, device=cuda_device).to(torch.bfloat16) for _ in range(3))
+        sigma = (torch.randint(0, 2, (D,), generator=g, device=cuda_device, dtype=torch.int32) * 2 - 1).to(torch.int8)
+        prep = api.fp8_prepare(q, k, v, sigma, batch=B)
+
+        def run():
+            api.fa_fp8_prep(q, k, v, prep["q8"], prep["k8"], prep["v8"], prep["q_scale"], prep["k_scale"],
+                            prep["v_scale"], sigma, B, H, S, S, D)
+        for _ in range(5):
+            run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(50):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 50
+        gbs = 3 * 3 * B * S * H * D / (ms * 1e-3) / 1e9
+        print(f"fa_fp8_prep D = {D:3d}: {ms * 1e3:7.1f} us per call, {gbs:7.0f} GB/s")
+        api.fa_get_device_status()
+        assert gbs > 0.0
