@@ -238,11 +238,16 @@ int launch16(fa::FwdLaunch& L, DevInfo* dev) {
 }
 
 // Key ranges of the split-KV forward. `requested` > 0 asks for that many;
-// `requested` <= 0 picks the count with the least estimated time, counting
-// whole waves of work tiles over the SMs times the 128-key blocks of one tile
-// plus a per-tile overhead of about four blocks (Q load, pipeline fill,
-// partial-result write), fewer ranges on ties. Work tiles come in whole
-// waves, so 9 ranges of 57 blocks in one wave beat 10 ranges in two.
+// `requested` <= 0 picks the count with the least estimated time, in units of
+// one SM's time for one 128-key block: whole waves of work tiles over the SMs
+// times (the blocks of one tile + about four blocks of per-tile overhead: Q
+// load, pipeline fill, output write; two more when the tile writes an fp32
+// partial O), plus, with more than one range, the merge, which moves every
+// range's partial O twice (written, then read) at about 12 MB of HBM traffic
+// per block time. Fewer ranges on ties. Work tiles come in whole waves, so 9
+// ranges of 57 blocks in one wave beat 10 ranges in two; a prefill whose
+// tiles already fill the SMs keeps one range, since the partials and their
+// merge cost more than the last wave's idle SMs.
 // Returns the ranges actually used (every range non-empty) and their length
 // in 128-key blocks.
 void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms, int* n_split,
@@ -254,7 +259,9 @@ void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms,
   if (n <= 0) {
     n = 1;
     if (tiles > 0 && sms > 0) {
-      const int64_t kOverhead = 4;
+      const int64_t kOverhead = 4, kPartialOverhead = 2;
+      const int64_t kMergeBytesPerBlock = (int64_t)12 << 20;
+      const int64_t partial_bytes = (int64_t)B * H * Sq * D * (int64_t)sizeof(float);   // one range's O
       int64_t best = -1;
       const int64_t top = nblocks < kMaxSplits ? nblocks : kMaxSplits;
       for (int64_t c = 1; c <= top; ++c) {
@@ -262,7 +269,8 @@ void resolve_splits(int B, int H, int Sq, int Sk, int D, int requested, int sms,
         const int64_t used = (nblocks + per - 1) / per;   // non-empty ranges
         if (used != c) continue;
         const int64_t waves = (tiles * c + sms - 1) / sms;
-        const int64_t cost = waves * (per + kOverhead);
+        int64_t cost = waves * (per + kOverhead + (c > 1 ? kPartialOverhead : 0));
+        if (c > 1) cost += (2 * c * partial_bytes + kMergeBytesPerBlock - 1) / kMergeBytesPerBlock;
         if (best < 0 || cost < best) {
           best = cost;
           n = c;
