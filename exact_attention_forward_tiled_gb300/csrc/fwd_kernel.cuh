@@ -24,7 +24,7 @@
 //       core busy while the two softmax warpgroups take turns (the ping-pong
 //       of the FlashAttention-3 wiki, technique 1, done with two tensor-memory
 //       score buffers instead of two register files).
-//   load warp (one thread)
+//   load warp (one thread; a whole warp, plus a V-load warp, for paged K/V)
 //       TMA loads of the Q tiles and of K_j, V_j into a ring of shared-memory
 //       slots guarded by full / empty mbarriers (producer / consumer of the
 //       wiki's technique 1; multi-stage K/V pipeline of technique 2). Paged
