@@ -134,6 +134,26 @@ def test_varlen_small(D, causal):
     _check(o, lse, o_ref, lse_ref, dtype, f"varlen D{D} causal={causal}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_runs_of_empty_tiles(D, causal):
+    """One long sequence among many one-token ones: most work tiles (the query
+    blocks a short sequence does not have) are empty, in runs longer than the
+    tile ring is deep, so every role must pass them without waiting on one
+    another. Every row against the oracle, and no device status raised."""
+    lens = [1] * 20 + [3000] + [1] * 20 + [200]
+    H = 4
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+    T = int(cu[-1])
+    dtype = torch.bfloat16
+    q, k, v = (_rand((T, H, D), dtype, 900 + i + D) for i in range(3))
+    o, lse = _run(q, k, v, causal=causal, scale=D ** -0.5, cu_seqlens_q=cu, cu_seqlens_k=cu,
+                  max_seqlen_q=max(lens), max_seqlen_k=max(lens))
+    o_ref, lse_ref = orc.attention(q.cpu(), k.cpu(), v.cpu(), scale=D ** -0.5, causal=causal,
+                                   nseq=len(lens), cu_seqlens_q=cu.cpu(), cu_seqlens_k=cu.cpu())
+    _check(o, lse, o_ref, lse_ref, dtype, f"varlen empty runs D{D} causal={causal}")
+
+
 def test_varlen_bad_seqlens_reported():
     """A cu_seqlens entry beyond total_q is caught by the kernel's own bounds
     check: the sequence is skipped and the status word reports it."""
