@@ -91,9 +91,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * tiles alone would not (short Sq, long Sk).
  *
  *   arguments as fa_fwd, fixed length only (no cu_seqlens)
- *   num_splits   key ranges; <= 0 picks about two work tiles per SM. It is
- *                capped at 256 and at ceil(Sk/128), and trimmed so that no
- *                range is empty.
+ *   num_splits   key ranges; <= 0 picks the count with the least estimated
+ *                time: whole waves of work tiles over the SMs, the key blocks
+ *                of a tile plus a per-tile overhead, and the merge of the
+ *                partial results (so a call whose tiles already fill the GPU
+ *                keeps one range). It is capped at 256 and at ceil(Sk/128),
+ *                and trimmed so that no range is empty.
  *   workspace    device scratch of at least
  *                fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits)
  *                bytes, 256-byte aligned, owned by the caller; its contents
