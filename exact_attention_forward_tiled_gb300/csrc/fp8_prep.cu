@@ -285,8 +285,10 @@ __global__ void __launch_bounds__(PrepCfg<D>::kThreads, PrepCfg<D>::kCtasPerSm)
       }
       return;
     }
-    // 1/sqrt(D) of the rotation is applied once, in the quantisation multiplier
-    const float norm = rot ? rsqrtf((float)D) : 1.f;
+    // 1/sqrt(D) of the rotation, rounded once to fp32 (exact for D = 64 and
+    // 256), is applied once, in the quantisation multiplier; every step of the
+    // code decision is then a correctly rounded fp32 operation
+    const float norm = rot ? (D == 64 ? 0.125f : D == 128 ? 0x1.6a09e6p-4f : 0.0625f) : 1.f;
     amax = red[0];
 #pragma unroll
     for (int i = 1; i < NW; ++i) amax = fmaxf(amax, red[i]);

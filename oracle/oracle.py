@@ -41,12 +41,9 @@ Parity status of each function (what pins it; see tests/test_oracle_*.py):
 * ``visible_pairs`` -- pinned: brute-force counts of tiny causal and
   non-causal cases.
 * ``e4m3_round`` -- decode of encode, both pinned above.
-* ``quantize_blocks`` -- pinned: idempotent, and every value within the e4m3
-  half-ulp bound (2^-4 relative) of its input.
-* ``block_scales`` / ``tensor_scale`` / ``fp8_attention_emulated`` -- parity
-  unpinned beyond the special cases in the tests: the block granularity, the
-  amax/448 scale and the rule that quantises P are readings of pages that
-  leave them open.
+
+The FP8 path (Hadamard rotation, block quantisation, e4m3 attention) has its
+own module, ``oracle/fp8.py``, with its parity status in its header.
 """
 from __future__ import annotations
 
@@ -468,88 +465,3 @@ def e4m3_encode(x) -> np.ndarray:
 def e4m3_round(x) -> np.ndarray:
     """x rounded to the nearest E4M3 value (encode then decode)."""
     return e4m3_decode(e4m3_encode(x))
-
-
-# --------------------------------------------------------------------------
-# FP8 emulations (block + Hadamard, and per-tensor), for error comparisons
-# --------------------------------------------------------------------------
-def block_scales(x, block=128) -> np.ndarray:
-    """One scale per block of ``block`` consecutive rows: amax / 448, or 1 when
-    the block is all zero. "FlashAttention-3 (lukebest wiki)" section 3:
-    block quantisation with an independent scale per tile. Reading: a tile is
-    128 rows of one (sequence, head), matching the kernel's 128-row tiles."""
-    x = _f64(x)
-    n = x.shape[0]
-    nb = (n + block - 1) // block
-    s = np.ones(nb)
-    for b in range(nb):
-        amax = np.abs(x[b * block:(b + 1) * block]).max() if n else 0.0
-        s[b] = amax / E4M3_MAX if amax > 0 else 1.0
-    return s
-
-
-def quantize_blocks(x, scales, block=128) -> np.ndarray:
-    """Dequantised value of e4m3(x / s_blk) * s_blk, row block by row block."""
-    x = _f64(x)
-    out = np.empty_like(x)
-    for b, s in enumerate(scales):
-        sl = slice(b * block, (b + 1) * block)
-        out[sl] = e4m3_round(x[sl] / s) * s
-    return out
-
-
-def fp8_attention_emulated(q, k, v, rows, *, scale, causal=False, mode="block_hadamard",
-                           sigma=None, tensor_scales=None, kappa=0, block=128):
-    """FP8 attention of one (sequence, head) pair, emulated in fp64.
-
-    mode ``"block_hadamard"`` ("FlashAttention-3 (lukebest wiki)" section 3):
-    Q' = QM, K' = KM with M = ``rotation(sigma)``; one scale per 128-row block
-    for Q', K' and V (V is not rotated); each operand is rounded to E4M3.
-
-    mode ``"per_tensor"``: no rotation, one scale per tensor, passed in
-    ``tensor_scales`` = (s_q, s_k, s_v) because it spans every head.
-
-    Both modes use the same rule for P: with m the row max of the dequantised
-    scores, P = exp(s - m), l = sum P (unrounded), P is rounded to E4M3 as
-    e4m3(P * 2^kappa) * 2^-kappa before it meets V. Returns O [len(rows), D]
-    for the query positions ``rows`` of this pair (non-causal unless asked).
-    """
-    q = _f64(q)
-    k = _f64(k)
-    v = _f64(v)
-    Lq, D = q.shape
-    Lk = k.shape[0]
-    if mode == "block_hadamard":
-        M = rotation(sigma)
-        qr, kr = q @ M, k @ M
-        qd = quantize_blocks(qr, block_scales(qr, block), block)
-        kd = quantize_blocks(kr, block_scales(kr, block), block)
-        vd = quantize_blocks(v, block_scales(v, block), block)
-    elif mode == "per_tensor":
-        sq, sk, sv = tensor_scales
-        qd = e4m3_round(q / sq) * sq
-        kd = e4m3_round(k / sk) * sk
-        vd = e4m3_round(v / sv) * sv
-    else:
-        raise ValueError(mode)
-    rows = np.asarray(rows, dtype=np.int64)
-    out = np.zeros((len(rows), D))
-    for n, i in enumerate(rows):
-        visible = Lk if not causal else min(Lk, int(i) + Lk - Lq + 1)
-        if visible <= 0:
-            continue
-        s = scale * (kd[:visible] @ qd[i])
-        p = np.exp(s - s.max())
-        l = p.sum()
-        p8 = e4m3_round(p * 2.0 ** kappa) * 2.0 ** -kappa
-        out[n] = (p8 @ vd[:visible]) / l
-    return out
-
-
-def tensor_scale(x) -> float:
-    """amax / 448 over a whole tensor (1 when it is all zero)."""
-    if hasattr(x, "detach"):
-        amax = float(x.detach().abs().max().to("cpu", dtype=__import__("torch").float64))
-    else:
-        amax = float(np.abs(np.asarray(x)).max())
-    return amax / E4M3_MAX if amax > 0 else 1.0

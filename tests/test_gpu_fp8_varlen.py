@@ -1,11 +1,12 @@
 """GPU parity of the variable-length FP8 path (fa_varlen_blocks,
 fa_fp8_prep_varlen, fa_fwd_fp8_varlen) through the C ABI.
 
-Same bars as the fixed-length FP8 tests: per sequence and head, scales within
-fp32 rounding of the oracle's and e4m3 codes at most one code apart; attention
-against the fp64 oracle on the dequantised inputs with a normalised RMSE of
-5 % and |LSE - LSE_ref| <= 1e-3. Where the varlen path and the fixed-length
-path see the same problem, they must agree bit for bit.
+Same bars as the fixed-length FP8 tests (``tests/test_gpu_fp8.py``): per
+sequence and head, codes and scales bit for bit against the FP8 oracle
+(``oracle/fp8.py``, decisions in fp32); attention element by element within
+twice the bounds of ``tests/fp8_bound.py`` and |LSE - LSE_ref| <= 1e-3. Where
+the varlen path and the fixed-length path see the same problem, they must
+agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,8 @@ import torch
 
 from exact_attention_forward_tiled_gb300 import api
 from exact_attention_forward_tiled_gb300 import build as fa_build
-from oracle import oracle as orc
+from oracle import fp8 as F
+from tests import fp8_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -42,33 +44,32 @@ def _blocks(lengths):
     return np.concatenate([[0], np.cumsum([(n + 127) // 128 for n in lengths])]).astype(np.int64)
 
 
-def _signed_index(codes):
-    c = codes.astype(np.int64)
-    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+def _seq_head(prep, name, lens, b, h):
+    """Codes [L_b, D] and scales [ceil(L_b / 128)] of sequence b, head h."""
+    start = int(np.sum(lens[:b]))
+    cb = _blocks(lens)
+    codes = prep[name + "8"][start:start + lens[b], h, :].cpu().numpy()
+    scales = prep[name + "_scale"][cb[b]:cb[b + 1], h].cpu().numpy()
+    return codes, scales
 
 
-def _oracle_prep(x, sigma):
-    x = orc._f64(x)
-    if sigma is not None:
-        x = x @ orc.rotation(sigma.cpu().numpy().astype(np.float64))
-    s = orc.block_scales(x)
-    codes = np.concatenate([orc.e4m3_encode(x[b * 128:(b + 1) * 128] / s[b]) for b in range(len(s))]) \
-        if len(s) else np.zeros((0, x.shape[1]), np.uint8)
-    return codes, s
-
-
-def _dequant(codes, scales, lengths):
-    """codes [total, H, D] e4m3, scales [n_blocks, H] -> fp64 values."""
-    val = orc.e4m3_decode(codes.cpu().numpy())
-    sc = scales.cpu().numpy()
-    cb = _blocks(lengths)
-    starts = np.concatenate([[0], np.cumsum(lengths)])
-    out = np.empty_like(val)
-    for b, n in enumerate(lengths):
-        for blk in range((n + 127) // 128):
-            r0, r1 = starts[b] + blk * 128, starts[b] + min(blk * 128 + 128, n)
-            out[r0:r1] = val[r0:r1] * sc[cb[b] + blk][None, :, None]
-    return out
+def _check_seqs(prep, o, lse, lq, lk, H, scale, causal):
+    """Every (sequence, head) with queries: element-wise against the oracle."""
+    starts = np.concatenate([[0], np.cumsum(lq)])
+    for b in range(len(lq)):
+        if lq[b] == 0:
+            continue
+        for h in range(H):
+            q8, qs = _seq_head(prep, "q", lq, b, h)
+            k8, ks = _seq_head(prep, "k", lk, b, h)
+            v8, vs = _seq_head(prep, "v", lk, b, h)
+            og = o[starts[b]:starts[b + 1], h, :].float().cpu().numpy()
+            lg = lse[h, starts[b]:starts[b + 1]].cpu().numpy()
+            if lk[b] == 0:
+                assert np.all(og == 0) and np.all(np.isneginf(lg))
+                continue
+            fp8_bound.check_attention(og, lg, q8, qs, k8, ks, v8, vs, np.arange(lq[b]), lq[b], scale=scale,
+                                      causal=causal)
 
 
 LQ = [1, 300, 128, 0, 257, 40]
@@ -78,7 +79,8 @@ LK = [129, 5, 400, 64, 0, 40]
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_varlen_blocks_and_prep_parity(D):
     """Block offsets match the host prefix sums; every sequence's blocks
-    (counted from its own first token, short last block) match the oracle."""
+    (counted from its own first token, short last block) match the oracle bit
+    for bit."""
     H = 3
     q = _rand((sum(LQ), H, D), 1, 2.0)
     k = _rand((sum(LK), H, D), 2)
@@ -91,24 +93,21 @@ def test_varlen_blocks_and_prep_parity(D):
     api.fa_get_device_status()
     assert np.array_equal(prep["cu_blocks_q"].cpu().numpy(), _blocks(LQ))
     assert np.array_equal(prep["cu_blocks_k"].cpu().numpy(), _blocks(LK))
-    for name, x, lens, sg in (("q", q, LQ, sigma), ("k", k, LK, sigma), ("v", v, LK, None)):
-        codes = prep[name + "8"].cpu().numpy()
-        scales = prep[name + "_scale"].cpu().numpy()
-        cb = _blocks(lens)
+    sg = sigma.cpu().numpy()
+    for name, x, lens, rot in (("q", q, LQ, sg), ("k", k, LK, sg), ("v", v, LK, None)):
         start = 0
         for b, n in enumerate(lens):
             for h in range(H):
-                ref_codes, ref_s = _oracle_prep(x[start:start + n, h, :].cpu(), sg)
-                np.testing.assert_allclose(scales[cb[b]:cb[b + 1], h], ref_s, rtol=2e-6, err_msg=name)
-                d = np.abs(_signed_index(codes[start:start + n, h, :]) - _signed_index(ref_codes))
-                if n:
-                    assert d.max() <= 1, (name, b, h)
+                ref_codes, ref_s = F.prepare(x[start:start + n, h, :].cpu(), rot)
+                codes, scales = _seq_head(prep, name, lens, b, h)
+                assert np.array_equal(scales, ref_s), (name, b, h)
+                assert np.array_equal(codes, ref_codes), (name, b, h)
             start += n
 
 
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_varlen_attention_matches_dequantized(D, causal):
+def test_fp8_varlen_attention_elementwise(D, causal):
     H = 2
     q = _rand((sum(LQ), H, D), 10)
     k = _rand((sum(LK), H, D), 11)
@@ -118,21 +117,10 @@ def test_fp8_varlen_attention_matches_dequantized(D, causal):
                                   max_seqlen_q=max(LQ), max_seqlen_k=max(LK))
     o, lse = api.fp8_attention_forward(prep, causal=causal)
     api.fa_get_device_status()
-    qd = _dequant(prep["q8"], prep["q_scale"], LQ)
-    kd = _dequant(prep["k8"], prep["k_scale"], LK)
-    vd = _dequant(prep["v8"], prep["v_scale"], LK)
-    o_ref, lse_ref = orc.attention(qd, kd, vd, scale=D ** -0.5, causal=causal, nseq=len(LQ),
-                                   cu_seqlens_q=cq.cpu().numpy(), cu_seqlens_k=ck.cpu().numpy())
-    o = o.float().cpu().numpy()
-    nrmse = np.linalg.norm(o - o_ref) / np.linalg.norm(o_ref)
-    assert nrmse <= 0.05, nrmse
-    l = lse.cpu().numpy()
-    fin = np.isfinite(lse_ref)
-    assert np.array_equal(np.isfinite(l), fin)
-    assert np.abs(l[fin] - lse_ref[fin]).max() <= 1e-3
+    _check_seqs(prep, o, lse, LQ, LK, H, D ** -0.5, causal)
     # rows with no visible key (the sequence with Lk = 0): O = 0
     s = sum(LQ[:4])
-    assert np.all(o[s:s + LQ[4]] == 0)
+    assert np.all(o[s:s + LQ[4]].float().cpu().numpy() == 0)
 
 
 def test_fp8_varlen_equals_fixed_length_bitwise():
@@ -184,17 +172,9 @@ def test_fp8_varlen_kv_prepared_once_and_reused():
                                  max_seqlen_q=max(lq), max_seqlen_k=0)
     o3, lse3 = api.fp8_attention_forward({**kv, **qq2}, causal=True)
     api.fa_get_device_status()
-    qd = _dequant(qq2["q8"], qq2["q_scale"], lq)
-    kd = _dequant(kv["k8"], kv["k_scale"], lk)
-    vd = _dequant(kv["v8"], kv["v_scale"], lk)
-    o_ref, lse_ref = orc.attention(qd, kd, vd, scale=D ** -0.5, causal=True, nseq=len(lq),
-                                   cu_seqlens_q=cq.cpu().numpy(), cu_seqlens_k=ck.cpu().numpy())
-    o3 = o3.float().cpu().numpy()
-    assert np.linalg.norm(o3 - o_ref) / np.linalg.norm(o_ref) <= 0.05
-    l3 = lse3.cpu().numpy()
-    fin = np.isfinite(lse_ref)   # causal rows of sequence 1 (Lq > Lk) see no key
-    assert np.array_equal(np.isfinite(l3), fin) and not fin.all()
-    assert np.abs(l3[fin] - lse_ref[fin]).max() <= 1e-3
+    _check_seqs({**kv, **qq2}, o3, lse3, lq, lk, H, D ** -0.5, True)
+    # causal rows of sequence 1 (Lq > Lk) that see no key
+    assert not torch.isfinite(lse3).all()
 
 
 def test_fp8_varlen_bad_block_offsets_are_reported():

@@ -1,10 +1,13 @@
-"""CPU tests of the oracle's Hadamard rotation, E4M3 codec and FP8 emulation."""
+"""CPU tests of the oracle's Hadamard rotation, E4M3 codec and FP8 path
+(``oracle/fp8.py``): every pin of ``tests/fp8_pins.py`` on the real module."""
 import numpy as np
 import pytest
 import scipy.linalg
 import torch
 
+from oracle import fp8 as F
 from oracle import oracle as O
+from tests.fp8_pins import ALL_PINS
 
 
 @pytest.mark.parametrize("D", [1, 2, 4, 8, 16, 32, 64, 128, 256])
@@ -65,42 +68,23 @@ def test_e4m3_saturates_and_nan():
     assert O.e4m3_encode(np.array([np.nan]))[0] == 0x7F
 
 
-def test_block_scales_map_amax_to_448():
-    r = np.random.default_rng(1)
-    x = r.standard_normal((300, 16)) * np.array([1.0] * 8 + [30.0] * 8)
-    x[256:] = 0.0
-    s = O.block_scales(x)
-    assert s.shape == (3,) and s[2] == 1.0
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_fp8_oracle_pin(pin):
+    pin(F)
+
+
+def test_fp8_prepare_decides_codes_in_fp32():
+    """The codes are the e4m3 rounding of fp32(y * multiplier): the same
+    values from torch's float8_e4m3fn cast of the fp32 products."""
+    r = np.random.default_rng(9)
+    D = 128
+    x = (r.standard_normal((256, D)) * 3).astype(np.float32)
+    x = (x.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    sigma = r.choice([-1.0, 1.0], size=D)
+    codes, scales = F.prepare(x, sigma)
+    y = F.fwht((x * sigma).astype(np.float32), np.float32)
+    norm = F.rotation_norm(D)
     for b in range(2):
-        blk = x[b * 128:(b + 1) * 128]
-        amax = np.abs(blk).max()
-        assert s[b] == amax / 448.0
-        assert O.e4m3_encode(np.array([amax / s[b]]))[0] == 0x7E
-    qd = O.quantize_blocks(x, s)
-    assert np.abs(qd - x).max() <= np.abs(x).max() * 2.0 ** -4 + 1e-12
-    again = O.quantize_blocks(qd, s)
-    assert np.array_equal(again, qd)
-
-
-def test_fp8_emulation_single_key_is_quantised_v():
-    """One key: P = 1 exactly, so O is V after its block quantisation."""
-    r = np.random.default_rng(2)
-    D = 64
-    q, k, v = r.standard_normal((4, D)), r.standard_normal((1, D)), r.standard_normal((1, D))
-    sigma = r.choice([-1.0, 1.0], size=D)
-    o = O.fp8_attention_emulated(q, k, v, np.zeros(4, dtype=np.int64), scale=0.125,
-                                 mode="block_hadamard", sigma=sigma, kappa=0)
-    vd = O.quantize_blocks(v, O.block_scales(v))
-    assert np.array_equal(o, np.tile(vd[0], (4, 1)))
-
-
-def test_fp8_emulation_close_to_exact_without_outliers():
-    r = np.random.default_rng(3)
-    L, D = 256, 128
-    q, k, v = (r.standard_normal((L, D)) for _ in range(3))
-    sigma = r.choice([-1.0, 1.0], size=D)
-    rows = np.arange(0, L, 7)
-    exact, _ = O.attention_head(q[rows], rows, k, v, L, D ** -0.5, False)
-    emu = O.fp8_attention_emulated(q, k, v, rows, scale=D ** -0.5, mode="block_hadamard", sigma=sigma)
-    rel = np.linalg.norm(emu - exact) / np.linalg.norm(exact)
-    assert rel < 0.1
+        mult = norm / scales[b]
+        prod = (y[b * 128:(b + 1) * 128] * mult).astype(np.float32)
+        assert np.array_equal(codes[b * 128:(b + 1) * 128], _torch_codes(prod))
