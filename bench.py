@@ -319,67 +319,6 @@ def run_reference(args):
     return 0
 
 
-def probe_link(nbytes=134217728, reps=10):
-    """Pinned host <-> device copy bandwidth (the bound of e2e): three
-    nbytes-sized tensors per measurement, one stream and chunked over several
-    streams, D2H alone and H2D beside a D2H. Prints one JSON line."""
-    import torch
-    dev = torch.device("cuda")
-    hs = [torch.ones(nbytes, dtype=torch.uint8).pin_memory() for _ in range(3)]
-    ds = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(3)]
-    oh = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-
-    def rate(fn, moved):
-        fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return moved * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
-
-    def h2d_chunked(ns):
-        sts = [torch.cuda.Stream() for _ in range(ns)]
-
-        def run():
-            cur = torch.cuda.current_stream()
-            step = nbytes // ns
-            for i, (d, h) in enumerate(zip(ds, hs)):
-                for c in range(ns):
-                    st = sts[(i * ns + c) % ns]
-                    st.wait_stream(cur)
-                    with torch.cuda.stream(st):
-                        d[c * step:(c + 1) * step].copy_(h[c * step:(c + 1) * step], non_blocking=True)
-            for st in sts:
-                cur.wait_stream(st)
-        return run
-
-    def d2h():
-        oh.copy_(ds[0], non_blocking=True)
-
-    s2 = torch.cuda.Stream()
-
-    def both():
-        cur = torch.cuda.current_stream()
-        s2.wait_stream(cur)
-        with torch.cuda.stream(s2):
-            oh.copy_(ds[1], non_blocking=True)
-        for d, h in zip(ds, hs):
-            d.copy_(h, non_blocking=True)
-        cur.wait_stream(s2)
-
-    out = {"probe": "host link", "unit": "GB/s", "bytes_per_copy": nbytes,
-           "h2d_1_stream": rate(h2d_chunked(1), 3 * nbytes)}
-    for ns in (2, 4, 8):
-        out[f"h2d_{ns}_streams"] = rate(h2d_chunked(ns), 3 * nbytes)
-    out["d2h_1_stream"] = rate(d2h, nbytes)
-    out["h2d_beside_d2h"] = rate(both, 3 * nbytes)
-    print(json.dumps(out), flush=True)
-    return 0
-
-
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -391,8 +330,6 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's number of sequences (smaller profiling cases)")
-    ap.add_argument("--probe-link", action="store_true",
-                    help="measure the pinned host <-> device copy bandwidth that bounds e2e and exit")
     ap.add_argument("--page-size", type=int, default=None,
                     help="paged workloads: override the page size; 0 runs the same shapes with contiguous K/V "
                          "through fa_fwd")
@@ -401,8 +338,6 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    if args.probe_link:
-        return probe_link()
 
     import torch
     import torch.distributed as dist
@@ -682,6 +617,17 @@ def main(argv=None):
             cb = oracle_bwd_sample(w, host, seconds=args.cpu_seconds)
         else:
             cb = oracle_sample(w, host, seconds=args.cpu_seconds)
+            # the same oracle on one host thread, over the first 512 rows of
+            # the first (sequence, head) pair
+            from oracle import oracle as orc
+            n_thr = orc.num_threads()
+            orc.set_num_threads(1)
+            try:
+                one = oracle_sample(w, host, seconds=0.0, max_rows=512)
+            finally:
+                orc.set_num_threads(n_thr)
+            cb["value_1_thread"] = one["value"]
+            cb["sample_1_thread"] = one["sample"].replace("with OpenMP", "on 1 thread")
         cb.pop("seconds")
         cb.pop("rows")
         line["cpu_baseline"] = cb

@@ -72,6 +72,32 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
     return LIB
 
 
+def build_variant(out_dir: str, defines, jobs: int | None = None) -> str:
+    """Compile every .cu under csrc/ with extra preprocessor ``defines`` into
+    ``out_dir`` and link ``libfa_variant.so`` there (the test build that
+    withholds a tile, FA_TEST_WITHHOLD_KV). The release library is untouched.
+    Returns the path of the variant library."""
+    os.makedirs(out_dir, exist_ok=True)
+    exe = nvcc()
+    flags = [f"-D{d}" for d in defines]
+
+    def compile_one(src):
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([exe, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    srcs = sources()
+    with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    lib = os.path.join(out_dir, "libfa_variant.so")
+    r = subprocess.run([exe, *ARCH, "-shared", "-cudart", "shared", "-o", lib, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

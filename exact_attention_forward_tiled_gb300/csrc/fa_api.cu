@@ -11,19 +11,27 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "sched_slots.h"
 
 // Device status word (one per device that loads the library): kernels OR in
 // fa::kDev* codes; fa_get_device_status() reads and clears it.
 __device__ int g_fa_status;
 
 // Tile-scheduler counters {next tile, CTAs done}, one pair per launch slot.
-// A launch takes the next slot in turn; its last CTA puts the pair back to
-// zero, so a slot is ready again once its launch has finished. Up to
-// kSchedSlots launches may be in flight on one device at the same time.
+// A launch takes a free slot (fa::SlotTable: never used, or its last launch
+// has finished, which an event recorded after that launch tells); its last
+// CTA puts the pair back to zero. Up to kSchedSlots launches may be in flight
+// on one device at the same time; one more is refused with FA_ERR_BUSY.
 constexpr int kSchedSlots = 64;
 __device__ unsigned int g_fa_sched[kSchedSlots][2];
 
 namespace {
+
+#ifdef FA_TEST_WITHHOLD_KV
+// test build only (fa_test_set_withhold): the key block whose K tile the
+// forward kernel's CTA 0 withholds, -1 for none
+std::atomic<int> g_test_withhold{-1};
+#endif
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 256;   // key ranges of the split-KV forward, at most
@@ -33,9 +41,9 @@ struct DevInfo {
   int sms = 0;
   int* status = nullptr;
   unsigned int* sched = nullptr;
-  std::atomic<unsigned int> next_slot{0};
-
-  unsigned int* take_slot() { return sched + 2 * (next_slot.fetch_add(1) % kSchedSlots); }
+  std::mutex slot_mu;                  // held from taking a slot to recording its event
+  fa::SlotTable<kSchedSlots> slots;
+  cudaEvent_t done_ev[kSchedSlots] = {};   // recorded on the stream after each slot's launch
 };
 
 std::mutex g_mu;
@@ -69,12 +77,60 @@ int current_device(DevInfo** out) {
       return FA_ERR_CUDA;
     }
     d.sched = static_cast<unsigned int*>(sym);
+    for (int i = 0; i < kSchedSlots; ++i) {
+      if (cudaEventCreateWithFlags(&d.done_ev[i], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        for (int j = 0; j < i; ++j) cudaEventDestroy(d.done_ev[j]);
+        return FA_ERR_CUDA;
+      }
+    }
     d.sms = sms;
     d.ready = true;
   }
   *out = &d;
   return FA_OK;
 }
+
+// One persistent launch's hold on a scheduler slot: the constructor takes a
+// free slot (sched == nullptr: all kSchedSlots held by launches in flight),
+// launched() records the slot's event after the launch went out. On a stream
+// that is being captured into a graph no event is recorded or queried (the
+// library does not see the graph's replays; the slot is handed out as free
+// again, and replays must not overlap other launches of the library).
+class SlotHold {
+ public:
+  SlotHold(DevInfo* dev, cudaStream_t stream) : dev_(dev), stream_(stream), lock_(dev->slot_mu) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      cs = cudaStreamCaptureStatusActive;
+    }
+    capturing_ = cs != cudaStreamCaptureStatusNone;
+    slot_ = dev->slots.take([dev](int i) {
+      const cudaError_t q = cudaEventQuery(dev->done_ev[i]);
+      if (q == cudaErrorNotReady) return false;
+      if (q != cudaSuccess) cudaGetLastError();
+      return true;
+    });
+    if (slot_ >= 0 && capturing_) dev->slots.release(slot_);
+  }
+  unsigned int* sched() const { return slot_ < 0 ? nullptr : dev_->sched + 2 * slot_; }
+  // the launch went out (ok) or failed
+  void launched(bool ok) {
+    if (slot_ < 0 || capturing_) return;
+    if (!ok || cudaEventRecord(dev_->done_ev[slot_], stream_) != cudaSuccess) {
+      cudaGetLastError();
+      if (!ok) dev_->slots.release(slot_);
+    }
+  }
+
+ private:
+  DevInfo* dev_;
+  cudaStream_t stream_;
+  std::lock_guard<std::mutex> lock_;
+  bool capturing_ = false;
+  int slot_ = -1;
+};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -127,7 +183,14 @@ int head_group(bool causal, int64_t BH, int64_t stream_rows, int D, int elem_byt
 
 extern "C" {
 
-int fa_version(void) { return (1 << 16) | 3; }
+#ifdef FA_TEST_WITHHOLD_KV
+// test build only: later 16-bit forward launches withhold the K tile of key
+// block kb in CTA 0's first work tile (kb < 0: none). Not in fa.h and not in
+// the release library.
+void fa_test_set_withhold(int kb) { g_test_withhold.store(kb); }
+#endif
+
+int fa_version(void) { return (1 << 16) | 4; }
 
 const char* fa_strerror(int s) {
   switch (s) {
@@ -140,6 +203,7 @@ const char* fa_strerror(int s) {
     case FA_ERR_DEVICE_SEQLENS: return "cu_seqlens entry out of bounds; sequence skipped";
     case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
     case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in 64 MiB array holds";
+    case FA_ERR_BUSY: return "all 64 scheduler slots of the device are held by launches still in flight";
     default: return "unknown status";
   }
 }
@@ -212,6 +276,9 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
   L.p.status = dev->status;
   L.p.n_split = 1;
   L.p.split_blocks = 1 << 30;
+#ifdef FA_TEST_WITHHOLD_KV
+  L.p.test_withhold_kb = g_test_withhold.load();
+#endif
   L.D = D;
   L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
   L.causal = causal != 0;
@@ -222,7 +289,8 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
 }
 
 int launch16(fa::FwdLaunch& L, DevInfo* dev) {
-  L.p.sched = dev->take_slot();
+  SlotHold hold(dev, L.stream);
+  if ((L.p.sched = hold.sched()) == nullptr) return FA_ERR_BUSY;
   L.p.head_group = head_group(L.causal, (int64_t)L.p.B * L.p.H, L.p.Sk, L.D, 2);
   cudaError_t e;
   switch (L.D) {
@@ -230,6 +298,7 @@ int launch16(fa::FwdLaunch& L, DevInfo* dev) {
     case 128: e = L.one_tile ? fa::launch_fwd_d128_q1(L) : fa::launch_fwd_d128(L); break;
     default: e = fa::launch_fwd_d256(L); break;
   }
+  hold.launched(e == cudaSuccess);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -346,7 +415,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                                           round256((size_t)n * B * Sq * H * D * sizeof(float)));
   if ((st = launch16(L, dev)) != FA_OK) return st;
   cudaError_t e = fa::launch_splitkv_merge(L.p.o_part, L.p.lse_part, o, lse, n, B, H, Sq, D,
-                                           dtype == FA_FP16, L.stream);
+                                           dtype == FA_FP16, dev->sms, L.stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -420,7 +489,7 @@ int fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const 
                                           round256((size_t)n * B * Sq * H * D * sizeof(float)));
   if ((st = launch16(L, dev)) != FA_OK) return st;
   cudaError_t e = fa::launch_splitkv_merge(L.p.o_part, L.p.lse_part, o, lse, n, B, H, Sq, D,
-                                           dtype == FA_FP16, L.stream);
+                                           dtype == FA_FP16, dev->sms, L.stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -552,7 +621,6 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   L.p.ntiles = (int)ntiles;
   L.p.c = (float)((double)scale * 1.4426950408889634);
   L.p.status = dev->status;
-  L.p.sched = dev->take_slot();
   L.p.n_split = 1;
   L.p.split_blocks = 1 << 30;
   L.p.q_scale = q_scale;
@@ -560,13 +628,19 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   L.p.v_scale = v_scale;
   L.p.nblk_q = (Sq + 127) / 128;
   L.p.nblk_k = (Sk + 127) / 128;
+#ifdef FA_TEST_WITHHOLD_KV
+  L.p.test_withhold_kb = -1;
+#endif
   L.D = D;
   L.kind = fa::kE4M3;
   L.causal = causal != 0;
   L.p.head_group = head_group(L.causal, (int64_t)B * H, Sk, D, 1);
   L.num_sms = dev->sms;
   L.stream = static_cast<cudaStream_t>(stream);
+  SlotHold hold(dev, L.stream);
+  if ((L.p.sched = hold.sched()) == nullptr) return FA_ERR_BUSY;
   cudaError_t e = D == 128 ? fa::launch_fwd_fp8_d128(L) : fa::launch_fwd_fp8_d256(L);
+  hold.launched(e == cudaSuccess);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -703,7 +777,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     L.p.c = (float)((double)scale * 1.4426950408889634);
     L.p.scale = scale;
     L.p.status = dev->status;
-    L.p.sched = dev->take_slot();
     L.D = D;
     L.kind = dtype == FA_FP16 ? fa::kF16 : fa::kBF16;
     L.causal = causal != 0;
@@ -712,7 +785,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     L.num_sms = dev->sms;
     L.stream = s;
     if (L.p.ntiles == 0) continue;
+    SlotHold hold(dev, s);
+    if ((L.p.sched = hold.sched()) == nullptr) return FA_ERR_BUSY;
     const cudaError_t e = D == 64 ? fa::launch_bwd_d64(L) : fa::launch_bwd_d128(L);
+    hold.launched(e == cudaSuccess);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_CUDA;

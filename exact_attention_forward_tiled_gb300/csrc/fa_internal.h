@@ -59,6 +59,9 @@ struct FwdParams {
   int page_shift;   // log2(page_size) for a power of two, else -1
   int n_kblk_tag;   // max_pages * page_size / 128 + 1: tags a (sequence, key block) pair
   int head_group;   // heads whose tiles are visited rank-major together (tile_order)
+#ifdef FA_TEST_WITHHOLD_KV
+  int test_withhold_kb;   // test build only: key block whose K tile CTA 0 never loads (-1: none)
+#endif
 };
 
 // Work tile w -> (sequence-head index bh, rank jj of the tile within its
@@ -110,7 +113,8 @@ cudaError_t launch_fwd_d64_q1(const FwdLaunch& L);
 cudaError_t launch_fwd_d128_q1(const FwdLaunch& L);
 cudaError_t launch_fwd_d256(const FwdLaunch& L);
 cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                                 int n_split, int B, int H, int Sq, int D, int out_fp16, cudaStream_t stream);
+                                 int n_split, int B, int H, int Sq, int D, int out_fp16, int num_sms,
+                                 cudaStream_t stream);
 cudaError_t launch_fwd_fp8_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
 

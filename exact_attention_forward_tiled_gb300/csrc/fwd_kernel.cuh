@@ -45,7 +45,6 @@
 #include <cstdint>
 #include <math_constants.h>
 
-#include "exp2_poly.h"
 #include "fa_internal.h"
 #include "pipeline.cuh"
 #include "ptx.cuh"
@@ -71,10 +70,6 @@ struct FwdCfg {
   // lazy-rescale threshold (log2 units) and, for e4m3, the power of two P is
   // scaled by before it is rounded (P * 2^kappa <= 2^(tau + kappa) = 256 < 448)
   static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
-  // share of the exponentials computed by the FMA-pipe polynomial instead of
-  // MUFU (two softmax warps share one sub-partition's MUFU, 8 lanes / cycle):
-  // every kPolyEvery-th pair of scores, 0 = none
-  static constexpr int kPolyEvery = 0;
   // softmax arithmetic on packed fp32 pairs (fma/add .f32x2) or scalar
   static constexpr bool kPacked = true;
   // P handed to the MMA warp in two halves of 64 keys (e4m3, where the MMAs
@@ -305,7 +300,15 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
   };
   // K or V tile of 128-key block kb (absolute within the sequence); a tile
   // of the other paged warp's tensor only takes its place in the slot order
+  bool first_tile = true;   // this CTA's first work tile (the test build's withheld tile)
   auto load_kv = [&](const CUtensorMap* m, const TileInfo& ti, int kb, bool act) -> bool {
+#ifdef FA_TEST_WITHHOLD_KV
+    // test build only: CTA 0 never loads the K tile of key block
+    // p.test_withhold_kb of its first work tile -- no expected bytes, no copy,
+    // so nothing can land later -- and the MMA thread's bounded wait for it
+    // runs out; the release build has no such path
+    if (act && m == tk && blockIdx.x == 0 && first_tile && kb == p.test_withhold_kb) act = false;
+#endif
     acted = (acted << 1) | (act ? 1u : 0u);
     if (!act) {
       ++kvc;
@@ -355,6 +358,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
       if (w < 0) break;
     }
     const TileInfo ti = tile_info<C::kRows, CAUSAL>(p, w);
+    first_tile = j == 0;
     if (ti.n_kv == 0) continue;
     if (MODE != 2) {
 #pragma unroll
@@ -694,14 +698,8 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
             lo = fmaf(s[j], c, -mu);
             hi = fmaf(s[j + 1], c, -mu);
           }
-          if (C::kPolyEvery > 0 && (j / 2) % C::kPolyEvery == C::kPolyEvery - 1) {
-            ptx::exp2_poly2(lo, hi, kExp2C0, kExp2C1, kExp2C2, kExp2C3);
-            s[j] = lo;
-            s[j + 1] = hi;
-          } else {
-            s[j] = ptx::ex2(lo);
-            s[j + 1] = ptx::ex2(hi);
-          }
+          s[j] = ptx::ex2(lo);
+          s[j + 1] = ptx::ex2(hi);
         }
         if (masked) {
           // zero the invisible keys after the exponent: with c = 0 their

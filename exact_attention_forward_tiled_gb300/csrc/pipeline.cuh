@@ -11,7 +11,13 @@
 
 namespace fa {
 
+#ifdef FA_TEST_WITHHOLD_KV
+// test build (see load_role): waits give up after 50 ms, so the test that
+// withholds a tile sees the timeout quickly
+constexpr uint64_t kWaitLimitNs = 50000000ull;
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+#endif
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Bounded mbarrier waits shared by all roles of a CTA.

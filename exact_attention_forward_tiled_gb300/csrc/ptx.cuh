@@ -259,26 +259,6 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// 2^x for two lanes on the FMA pipe instead of MUFU: n = round(x) via the
-// 1.5 * 2^23 rounding trick, f = x - n in [-1/2, 1/2], 2^f by the fitted cubic
-// of exp2_poly.h, 2^n added straight into the exponent field. x is clamped to
-// -125 so the exponent stays in range (2^-125 stands for 0 here).
-__device__ __forceinline__ void exp2_poly2(float& a, float& b, float c0, float c1, float c2, float c3) {
-  const uint64_t x = f2pack(fmaxf(a, -125.f), fmaxf(b, -125.f));
-  const uint64_t magic = f2pack(12582912.f, 12582912.f);
-  const uint64_t t = add2(x, magic);
-  const uint64_t n = add2(t, f2pack(-12582912.f, -12582912.f));
-  const uint64_t f = fma2(n, f2pack(-1.f, -1.f), x);
-  uint64_t p = fma2(f, f2pack(c3, c3), f2pack(c2, c2));
-  p = fma2(p, f, f2pack(c1, c1));
-  p = fma2(p, f, f2pack(c0, c0));
-  float pa, pb, ta, tb;
-  f2unpack(p, pa, pb);
-  f2unpack(t, ta, tb);
-  a = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-  b = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
-}
-
 // four fp32 -> four e4m3 codes (round to nearest even, saturate to +-448) in
 // one word, a in the low byte: both pair conversions write 16-bit halves that
 // are joined without a shift or an or

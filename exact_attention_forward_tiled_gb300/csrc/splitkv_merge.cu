@@ -74,11 +74,14 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restr
 }
 
 cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                                 int n_split, int B, int H, int Sq, int D, int out_fp16, cudaStream_t stream) {
+                                 int n_split, int B, int H, int Sq, int D, int out_fp16, int num_sms,
+                                 cudaStream_t stream) {
   const int64_t total = (int64_t)B * Sq * H * (D / 4);
   if (total == 0) return cudaSuccess;
+  // grid-stride: at most 64 blocks of 256 threads per SM
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 64) blocks = 152 * 64;
+  const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 1) * 64;
+  if (blocks > cap) blocks = cap;
   if (out_fp16)
     splitkv_merge_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(o_part, lse_part, o, lse, n_split, B, H, Sq, D);
   else

@@ -17,8 +17,9 @@
 namespace {
 
 // The scratch: one fixed array per device that loads the library, held until
-// the process exits. 64 MiB covers, for example, 19 key ranges of
-// B=2 x H=8 x 256 query rows at D=128.
+// the process exits. A problem fits when fa_fwd_splitkv_workspace_size(...)
+// is at most 64 MiB: for example 31 key ranges of B=2 x H=8 x 256 query rows
+// at D=128 (each range 2 MiB of fp32 partial O and 16 KiB of partial LSE).
 constexpr size_t kScratchBytes = 64ull << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kScratchBytes];
 
@@ -28,7 +29,9 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device, looked up once per
 // device. In host code the array's name is only a stand-in, so the address
-// must come from cudaGetSymbolAddress with that device current.
+// must come from cudaGetSymbolAddress with that device current. The cached
+// address does not survive cudaDeviceReset (the library is not to be called
+// on a device after a reset).
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

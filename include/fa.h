@@ -26,9 +26,28 @@
  *     by the return value, errors found on the device by
  *     fa_get_device_status().
  *   - Return value: FA_OK (0) or a negative FA_ERR_* code (fa_strerror()).
- *   - The library allocates no memory. Its only device state is a status
- *     word and a small set of tile-scheduler counters per device (static
- *     __device__ variables); scratch that a call needs is passed in.
+ *   - The library allocates no device memory: scratch that a call needs is
+ *     passed in. Its device state, present on every device that loads the
+ *     library until the process exits, is static __device__ arrays: one
+ *     status word, 64 pairs of tile-scheduler counters, and the fixed 64 MiB
+ *     scratch array that only fa_fwd_splitkv_noalloc (below) uses.
+ *   - The first call on a device sets up the library's host-side state for it:
+ *     it looks up the device addresses of those arrays and creates one CUDA
+ *     event per scheduler slot (64). Make that first call before any stream
+ *     capture. The addresses are kept for the life of the process; they do
+ *     not survive cudaDeviceReset, so do not call the library on a device
+ *     after resetting it.
+ *   - Concurrency: every kernel that schedules work tiles dynamically holds
+ *     one of the device's 64 scheduler slots until it finishes (an event
+ *     recorded after its launch says when). At most 64 such launches may be
+ *     in flight on a device at once, over all streams and host threads; one
+ *     more is refused with FA_ERR_BUSY and nothing is launched. A launch
+ *     captured into a CUDA graph keeps the slot it was given at capture time
+ *     for every replay, unseen by the library: replays must not overlap one
+ *     another or other launches of the library on that device.
+ *   - The status word is per device, not per stream or call:
+ *     fa_get_device_status() reports (and clears) what any kernel of the
+ *     library on that device recorded since the last read.
  */
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
@@ -48,6 +67,7 @@ extern "C" {
 #define FA_ERR_DEVICE_SEQLENS -6  /* a cu_seqlens entry broke its bounds       */
 #define FA_ERR_NO_DEVICE -7       /* no sm_100-family device is current        */
 #define FA_ERR_SCRATCH_LIMIT -8   /* needs more than the built-in scratch      */
+#define FA_ERR_BUSY -9            /* 64 launches already in flight on device   */
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
 
@@ -124,8 +144,10 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * Returns FA_ERR_SCRATCH_LIMIT, before touching any pointer, when
  * fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, num_splits) exceeds 64 MiB
  * (ask for fewer key ranges, or use fa_fwd_splitkv). The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress); make
- * that first call before any stream capture. All calls share the one array:
+ * device looks up the array's device address (cudaGetSymbolAddress) and, if
+ * no other entry point has run on the device yet, sets up the library's
+ * per-device state (see the conventions above); make that first call before
+ * any stream capture. All calls share the one array:
  * calls that overlap on the GPU (other streams, other threads) race and give
  * wrong results. Nothing in it needs clearing between calls: every byte a
  * call reads, the same call has written. Allocates nothing.
@@ -325,7 +347,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 
 /*
  * fa_get_device_status -- synchronise `stream`, then read and clear the
- * current device's status word. Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a
+ * current device's status word (shared by every stream and call on the
+ * device: a code may come from a kernel on another stream). Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a
  * kernel's bounded wait expired; the kernel left early and its outputs are
  * incomplete), FA_ERR_DEVICE_SEQLENS, or FA_ERR_CUDA. `raw` (may be NULL)
  * receives the raw word for diagnosis.

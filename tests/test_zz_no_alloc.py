@@ -55,3 +55,23 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = api.fa_fwd_splitkv_noalloc(t, t, t, t, lse, B, H, Sq, Sk, D, 0.0625, 0, 16, check=False)
     assert st == -8
     assert "scratch" in api.strerror(st)
+
+
+def test_noalloc_near_its_limit():
+    """A problem whose scratch is just under the 64 MiB array (63 key ranges
+    of 1 MiB of partial O each; the partial LSE then sits in the last MiB):
+    the same result as fa_fwd_splitkv with a caller workspace."""
+    B, H, Sq, Sk, D, splits = 1, 8, 256, 8000, 128, 63
+    need = api.fa_fwd_splitkv_workspace_size(B, H, Sq, Sk, D, splits)
+    assert (63 << 20) < need <= (64 << 20), need
+    q = _rand((B * Sq, H, D), 31)
+    k = _rand((B * Sk, H, D), 32)
+    v = _rand((B * Sk, H, D), 33)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), device="cuda")
+    api.fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Sq, Sk, D, D ** -0.5, True, splits)
+    api.fa_get_device_status()
+    o_ref, lse_ref = api.attention_forward_splitkv(q, k, v, batch=B, causal=True, num_splits=splits)
+    api.fa_get_device_status()
+    assert (o.float() - o_ref.float()).abs().max().item() <= 1e-2
+    assert (lse - lse_ref).abs().max().item() <= 1e-3
