@@ -260,6 +260,7 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
   if ((st = make_map(&L.tq, q, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
   if ((st = make_map(&L.tk, k, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
   if ((st = make_map(&L.tv, v, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.to, o, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
   L.p.o = o;
   L.p.lse = lse;
   L.p.cu_q = cu_seqlens_q;
@@ -605,6 +606,8 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   if ((st = make_map(&L.tq, q8, dt, 1, cols, (uint64_t)Tq, 128, 128)) != FA_OK) return st;
   if ((st = make_map(&L.tk, k8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
   if ((st = make_map(&L.tv, v8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK)
+    return st;
   L.p.o = o;
   L.p.lse = lse;
   L.p.cu_q = cu_q;

@@ -91,6 +91,7 @@ enum Kind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 // Per-launch description filled by the front end.
 struct FwdLaunch {
   CUtensorMap tq, tk, tv;
+  CUtensorMap to;   // O [tokens, H * D], 16-bit, boxes of 64 x 128 with the 128-byte swizzle (TMA stores)
   FwdParams p;
   int D;
   int kind;  // Kind

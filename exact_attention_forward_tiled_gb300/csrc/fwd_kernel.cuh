@@ -96,7 +96,17 @@ struct FwdCfg {
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = QT * kTileBytes;
-  static constexpr int kOffBar = kOffKV + STAGES * kTileBytes;
+  // O leaves through shared memory and TMA stores (a 128-row x 64-column
+  // 16-bit box per softmax warpgroup, 128-byte swizzle) when the query tile
+  // is whole. Kept out of: the one-tile configurations of short query
+  // sequences (decode), whose tiles are almost never whole and whose K/V ring
+  // fills shared memory, and the e4m3 kernel, whose per-thread epilogue with
+  // four chunk loads under one wait measured faster (same box, c5 attention
+  // 1660 against 1638 TFLOP/s; 16-bit c2 1433 -> 1451, c4 1244 -> 1263)
+  static constexpr bool kTmaStore = !kFp8 && (QT == 2 || D == 256);
+  static constexpr int kEpiBytes = 128 * 128;
+  static constexpr int kOffEpi = kOffKV + STAGES * kTileBytes;
+  static constexpr int kOffBar = kOffEpi + (kTmaStore ? QT * kEpiBytes : 0);
   // barriers: q_full[2], q_empty[2] (per query tile, so the next work tile's
   // first Q tile loads while this one's last MMAs run), kv_full[S], kv_empty[S], s_full[2],
   // p_full[2][2] (per score buffer, first / second half of the keys),
@@ -543,9 +553,17 @@ __device__ __forceinline__ uint32_t pack_p16(float lo, float hi) {
   return KIND == kF16 ? ptx::pack_f16(lo, hi) : ptx::pack_bf16(lo, hi);
 }
 
+// one warpgroup's named barrier (ids 1, 2; 0 is __syncthreads)
+__device__ __forceinline__ void wg_sync(int t) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 template <class C, bool CAUSAL>
-__device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Waiter& wt,
-                             const TileRing& ring, int t, int quarter) {
+__device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t sbase, uint32_t tmem,
+                             const Waiter& wt, const TileRing& ring, int t, int quarter) {
   const uint32_t bars = sbase + C::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   const int lane = threadIdx.x & 31;
@@ -560,14 +578,22 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     if (!ti.live) continue;
     const int row = ti.q0 + 128 * t + r;
     const bool row_ok = row < ti.Lq;
-    const int64_t tok = (int64_t)ti.qtok + row;
     const bool split = p.o_part != nullptr;
-    uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + ti.h) * C::D;
-    float* oprow = split ? p.o_part + (((int64_t)ti.split * p.total_q + tok) * p.H + ti.h) * C::D : nullptr;
-    float* lse_ptr = split ? p.lse_part + (((int64_t)ti.split * p.B + ti.b) * p.H + ti.h) * p.Sq + row
-                     : p.cu_q != nullptr ? p.lse + (int64_t)ti.h * p.total_q + tok
-                                         : p.lse + ((int64_t)ti.b * p.H + ti.h) * p.Sq + row;
+    // this row's outputs (formed where they are written, so that they are not
+    // held in registers across the key loop)
+    auto out_ptrs = [&](uint16_t*& orow, float*& oprow, float*& lse_ptr) {
+      const int64_t tok = (int64_t)ti.qtok + row;
+      orow = reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + ti.h) * C::D;
+      oprow = split ? p.o_part + (((int64_t)ti.split * p.total_q + tok) * p.H + ti.h) * C::D : nullptr;
+      lse_ptr = split ? p.lse_part + (((int64_t)ti.split * p.B + ti.b) * p.H + ti.h) * p.Sq + row
+                : p.cu_q != nullptr ? p.lse + (int64_t)ti.h * p.total_q + tok
+                                    : p.lse + ((int64_t)ti.b * p.H + ti.h) * p.Sq + row;
+    };
     if (ti.n_kv == 0) {
+      uint16_t* orow;
+      float* oprow;
+      float* lse_ptr;
+      out_ptrs(orow, oprow, lse_ptr);
       // no visible key for any row of this block (or of this key range):
       // O = 0, LSE = -inf
       if (row_ok) {
@@ -758,43 +784,83 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
     ptx::tc_fence_after();
     const float inv_l = l > 0.f ? (C::kFp8 ? v_ref / (C::kKappaScale * l) : 1.f / l) : 0.f;
     const uint32_t o_addr = tl + C::col_o(C::QT == 2 ? t : 0);
-    // O leaves tensor memory in 32-column chunks. e4m3: batches of up to four
-    // chunks whose loads are issued back to back under one wait (the next
-    // work tile's first P of this warpgroup waits for this epilogue; measured
-    // on one box, c5 attention 1637 -> 1661 TFLOP/s); 16-bit: one chunk per
-    // wait (batching cost c2 1435 -> 1392 there)
-    constexpr int kBatch = !C::kFp8 ? 1 : (C::D / 32 < 4 ? C::D / 32 : 4);
+    uint16_t* orow;
+    float* oprow;
+    float* lse_ptr;
+    out_ptrs(orow, oprow, lse_ptr);
+    if (C::kTmaStore && !split && ti.q0 + 128 * t + 128 <= ti.Lq) {
+      // a whole query tile: O / l in 16 bits, 64 columns at a time, written
+      // row by row into this warpgroup's staging box in the 128-byte swizzle
+      // (16-byte chunk c of row r at chunk c ^ (r & 7)), then one TMA store;
+      // thread 0 of the warpgroup issues the stores and, before the box is
+      // reused, waits until the previous store has read it
+      const uint32_t stage = sbase + C::kOffEpi + (uint32_t)t * C::kEpiBytes;
+      const bool lead = quarter == 0 && lane == 0;
 #pragma unroll 1
-    for (int cb = 0; cb < C::D / 32; cb += kBatch) {
-      uint32_t v[kBatch][32];
+      for (int hb = 0; hb < C::D / 64; ++hb) {
+        if (lead) ptx::bulk_wait_read_all();
+        wg_sync(t);
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) ptx::tmem_ld32(o_addr + 32 * (cb + q), v[q]);
-      ptx::tmem_wait_ld();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          ptx::tmem_ld32(o_addr + 64 * hb + 32 * half, v);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(v);
+          uint32_t pk[16];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        ptx::reg_fence(v[q]);
-        const int ch = cb + q;
-        if (split) {
-          // partial O of this key range, fp32, normalised by its own l
-          if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(oprow + 32 * ch);
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_out<C::KIND>(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4)
-              dst[k4] = make_float4(__uint_as_float(v[q][4 * k4]) * inv_l, __uint_as_float(v[q][4 * k4 + 1]) * inv_l,
-                                    __uint_as_float(v[q][4 * k4 + 2]) * inv_l,
-                                    __uint_as_float(v[q][4 * k4 + 3]) * inv_l);
-          }
-          continue;
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(stage + (uint32_t)r * 128u + ((uint32_t)((4 * half + c) ^ (r & 7)) << 4), pk[4 * c],
+                         pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
-        uint32_t pk[16];
+        ptx::fence_proxy_async_smem();
+        wg_sync(t);
+        if (lead) {
+          ptx::tma_store_2d(to, stage, ti.h * C::D + 64 * hb, ti.qtok + ti.q0 + 128 * t);
+          ptx::bulk_commit();
+        }
+      }
+    } else {
+      // O leaves tensor memory in 32-column chunks. e4m3: batches of up to four
+      // chunks whose loads are issued back to back under one wait (the next
+      // work tile's first P of this warpgroup waits for this epilogue; measured
+      // on one box, c5 attention 1637 -> 1661 TFLOP/s); 16-bit: one chunk per
+      // wait (batching cost c2 1435 -> 1392 there)
+      constexpr int kBatch = !C::kFp8 ? 1 : (C::D / 32 < 4 ? C::D / 32 : 4);
+#pragma unroll 1
+      for (int cb = 0; cb < C::D / 32; cb += kBatch) {
+        uint32_t v[kBatch][32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_out<C::KIND>(__uint_as_float(v[q][2 * j]) * inv_l, __uint_as_float(v[q][2 * j + 1]) * inv_l);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+        for (int q = 0; q < kBatch; ++q) ptx::tmem_ld32(o_addr + 32 * (cb + q), v[q]);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            dst[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+        for (int q = 0; q < kBatch; ++q) {
+          ptx::reg_fence(v[q]);
+          const int ch = cb + q;
+          if (split) {
+            // partial O of this key range, fp32, normalised by its own l
+            if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(oprow + 32 * ch);
+#pragma unroll
+              for (int k4 = 0; k4 < 8; ++k4)
+                dst[k4] = make_float4(__uint_as_float(v[q][4 * k4]) * inv_l, __uint_as_float(v[q][4 * k4 + 1]) * inv_l,
+                                      __uint_as_float(v[q][4 * k4 + 2]) * inv_l,
+                                      __uint_as_float(v[q][4 * k4 + 3]) * inv_l);
+            }
+            continue;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_out<C::KIND>(__uint_as_float(v[q][2 * j]) * inv_l, __uint_as_float(v[q][2 * j + 1]) * inv_l);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              dst[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+          }
         }
       }
     }
@@ -808,7 +874,8 @@ __device__ void softmax_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, 
 template <int D, int QT, int STAGES, int KIND, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                  const FwdParams p) {
   using C = FwdCfg<D, QT, STAGES, KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -833,6 +900,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     ptx::prefetch_tmap(&tq);
     ptx::prefetch_tmap(&tk);
     ptx::prefetch_tmap(&tv);
+    if (C::kTmaStore) ptx::prefetch_tmap(&to);
   }
   if (warp == C::kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_holder), C::kTmemCols);
@@ -861,7 +929,9 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     }
   } else {
     if constexpr (C::kRebalance) ptx::setmaxnreg_inc<C::kRegsHigh>();
-    softmax_role<C, CAUSAL>(p, sbase, tmem, wt, ring, warp >> 2, warp & 3);
+    softmax_role<C, CAUSAL>(p, &to, sbase, tmem, wt, ring, warp >> 2, warp & 3);
+    // every O store this warpgroup issued has completed before the CTA ends
+    if (C::kTmaStore && (threadIdx.x & 127) == 0) ptx::bulk_wait_all();
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -888,7 +958,7 @@ cudaError_t launch_fwd_kind(const FwdLaunch& L) {
   if (e != cudaSuccess) return e;
   int grid = L.p.ntiles < L.num_sms ? L.p.ntiles : L.num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tq, L.tk, L.tv, L.p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tq, L.tk, L.tv, L.to, L.p);
   return cudaGetLastError();
 }
 
