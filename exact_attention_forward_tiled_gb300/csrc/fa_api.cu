@@ -577,7 +577,7 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
                  const float* v_scale, void* o, float* lse, int B, int H, int Sq, int Sk, int D, float scale,
                  int causal, const int* cu_q, const int* cu_k, const int* cbq, const int* cbk, int total_q,
                  int total_k, void* stream) {
-  if (D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -603,9 +603,13 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   std::memset(&L, 0, sizeof(L));
   const uint64_t cols = (uint64_t)H * D;
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if ((st = make_map(&L.tq, q8, dt, 1, cols, (uint64_t)Tq, 128, 128)) != FA_OK) return st;
-  if ((st = make_map(&L.tk, k8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
-  if ((st = make_map(&L.tv, v8, dt, 1, cols, (uint64_t)Tk, 128, 128)) != FA_OK) return st;
+  // boxes of 128 rows x 128 bytes (128-byte swizzle), or of one whole
+  // 64-byte row (64-byte swizzle) at D = 64
+  const uint32_t box = D == 64 ? 64u : 128u;
+  const CUtensorMapSwizzle sw = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  if ((st = make_map(&L.tq, q8, dt, 1, cols, (uint64_t)Tq, box, 128, sw)) != FA_OK) return st;
+  if ((st = make_map(&L.tk, k8, dt, 1, cols, (uint64_t)Tk, box, 128, sw)) != FA_OK) return st;
+  if ((st = make_map(&L.tv, v8, dt, 1, cols, (uint64_t)Tk, box, 128, sw)) != FA_OK) return st;
   if ((st = make_map(&L.to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK)
     return st;
   L.p.o = o;
@@ -642,7 +646,9 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   L.stream = static_cast<cudaStream_t>(stream);
   SlotHold hold(dev, L.stream);
   if ((L.p.sched = hold.sched()) == nullptr) return FA_ERR_BUSY;
-  cudaError_t e = D == 128 ? fa::launch_fwd_fp8_d128(L) : fa::launch_fwd_fp8_d256(L);
+  cudaError_t e = D == 64    ? fa::launch_fwd_fp8_d64(L)
+                  : D == 128 ? fa::launch_fwd_fp8_d128(L)
+                             : fa::launch_fwd_fp8_d256(L);
   hold.launched(e == cudaSuccess);
   if (e != cudaSuccess) {
     cudaGetLastError();

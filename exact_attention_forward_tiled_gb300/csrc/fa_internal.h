@@ -116,6 +116,7 @@ cudaError_t launch_fwd_d256(const FwdLaunch& L);
 cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                                  int n_split, int B, int H, int Sq, int D, int out_fp16, int num_sms,
                                  cudaStream_t stream);
+cudaError_t launch_fwd_fp8_d64(const FwdLaunch& L);
 cudaError_t launch_fwd_fp8_d128(const FwdLaunch& L);
 cudaError_t launch_fwd_fp8_d256(const FwdLaunch& L);
 

@@ -60,9 +60,13 @@ struct FwdCfg {
   static constexpr bool kFp8 = KIND == kE4M3;
   static constexpr int EB = kFp8 ? 1 : 2;          // bytes per input element
   static constexpr int kRows = 128 * QT;            // query rows per work tile
-  static constexpr int kBoxCols = 128 / EB;         // elements per 128-byte box row
+  // a tile is D / kBoxCols TMA boxes of 128 rows; a box row is 128 bytes in
+  // the 128-byte swizzle, or 64 bytes in the 64-byte swizzle when a whole row
+  // is 64 bytes (e4m3 at D = 64)
+  static constexpr int kRowBytes = D * EB < 128 ? D * EB : 128;   // bytes per box row
+  static constexpr int kBoxCols = kRowBytes / EB;   // elements per box row
   static constexpr int kBoxes = D / kBoxCols;       // boxes per 128-row tile
-  static constexpr int kBoxBytes = 128 * 128;       // one box: 128 rows x 128 bytes
+  static constexpr int kBoxBytes = 128 * kRowBytes; // one box: 128 rows
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kQkSteps = D * EB / 32;      // MMA K steps (32 bytes each) over D
   static constexpr int kKeysPerStep = 32 / EB;      // keys per PV MMA step
@@ -123,7 +127,8 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
 
   static_assert(D == 64 || D == 128 || D == 256, "head dimension");
-  static_assert(D % kBoxCols == 0, "a 128-row tile must be whole 128-byte boxes");
+  static_assert(kRowBytes == 128 || kRowBytes == 64, "box rows of 128 or 64 bytes");
+  static_assert(D % kBoxCols == 0, "a 128-row tile must be whole boxes");
   static_assert(QT == 1 || 2 * 128 + QT * D <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -343,7 +348,7 @@ __device__ void load_role(const CUtensorMap* tq, const CUtensorMap* tk, const CU
       if (my_box) {
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
-          ptx::tma_load_2d(dst + bx * C::kBoxBytes + lane * p.page_rows * 128, m, ti.h * C::D + bx * C::kBoxCols,
+          ptx::tma_load_2d(dst + bx * C::kBoxBytes + lane * p.page_rows * C::kRowBytes, m, ti.h * C::D + bx * C::kBoxCols,
                            row, b);
       }
     }
@@ -428,9 +433,10 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
   auto qk = [&](uint32_t s_col, uint32_t q_addr, uint32_t k_addr) {
 #pragma unroll
     for (int kk = 0; kk < C::kQkSteps; ++kk) {
-      const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-      const uint64_t a = ptx::smem_desc_sw128(q_addr + off, 16, 1024);
-      const uint64_t b = ptx::smem_desc_sw128(k_addr + off, 16, 1024);
+      constexpr int kStepsPerBox = C::kRowBytes / 32;
+      const uint32_t off = (kk / kStepsPerBox) * C::kBoxBytes + (kk % kStepsPerBox) * 32;
+      const uint64_t a = ptx::smem_desc_sw<C::kRowBytes>(q_addr + off, 16, 8 * C::kRowBytes);
+      const uint64_t b = ptx::smem_desc_sw<C::kRowBytes>(k_addr + off, 16, 8 * C::kRowBytes);
       if (C::kFp8)
         ptx::mma_f8_ss(tmem + s_col, a, b, idesc_qk, kk > 0);
       else
@@ -447,8 +453,8 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         if (!wt.wait(bar(C::kBarPFull + 2 * pbuf + (kk == 0 ? 0 : 1)), parity, 5)) return false;
         ptx::tc_fence_after();
       }
-      const uint64_t b =
-          ptx::smem_desc_sw128(v_addr + kk * C::kKeysPerStep * 128, C::kBoxBytes, 1024);
+      const uint64_t b = ptx::smem_desc_sw<C::kRowBytes>(v_addr + kk * C::kKeysPerStep * C::kRowBytes,
+                                                         C::kBoxBytes, 8 * C::kRowBytes);
       const uint32_t en = (acc || kk > 0) ? 1u : 0u;
       if (C::kFp8)
         ptx::mma_f8_ts(tmem + o_col, tmem + p_col + kk * 8, b, idesc_pv, en);

@@ -314,6 +314,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same for a tile whose rows are `row_bytes` = 128 or 64 bytes, stored in
+// the matching swizzle (128-byte: mode 2, atoms of 8 rows x 128 bytes; 64-byte:
+// mode 4, atoms of 8 rows x 64 bytes -- the layout TMA writes with
+// SWIZZLE_64B).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "swizzle width");
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(ROW_BYTES == 128 ? 2 : 4) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 / kind::f8f6f4 (dense, fp32 accumulator):
 //   bits 4-5 accumulator format (1 = f32); bits 7-9 / 10-12 A / B format
 //   (f16 kind: 0 = f16, 1 = bf16; f8f6f4 kind: 0 = e4m3); bit 15 / 16 A / B

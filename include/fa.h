@@ -234,7 +234,8 @@ int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype,
  *
  *   q8, k8, v8 and the three scale arrays as written by fa_fp8_prep
  *   o            bf16 [B*Sq, H, D] (written); lse fp32 [B, H, Sq] (written)
- *   D            128 or 256 (64 -> FA_ERR_UNSUPPORTED)
+ *   D            64, 128 or 256 (at D = 64 a 64-byte row of codes is one
+ *                TMA box in the 64-byte swizzle)
  *   scale, causal as for fa_fwd. Fixed length (varlen: fa_fwd_fp8_varlen).
  */
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
@@ -293,7 +294,7 @@ int fa_fp8_prep_varlen(const void* q, const void* k, const void* v, int in_dtype
  *   o            bf16 [total_q, H, D] (written); lse fp32 [H, total_q]
  *                (written)
  *   cu_*, total_*, max_seqlen_* as for fa_fp8_prep_varlen (all required)
- *   D            128 or 256; scale, causal as for fa_fwd (the causal
+ *   D            64, 128 or 256; scale, causal as for fa_fwd (the causal
  *                diagonal is bottom-right aligned per sequence)
  *
  * Bad sequences are skipped (their rows left unwritten) and reported as

@@ -81,7 +81,7 @@ def test_fp8_varlen_host_argument_checks(L):
     # every cu_seqlens / cu_blocks array is required by the forward
     for kw in ("cq", "ck", "cbq", "cbk"):
         assert _fp8_varlen(L, **{kw: None}) == -1, kw
-    assert _fp8_varlen(L, D=64) == -2
+    assert _fp8_varlen(L, D=96) == -2                # head sizes 64, 128, 256 only
     assert _fp8_varlen(L, tq=-1) == -1 and _fp8_varlen(L, scale=-2.0) == -1
     assert _fp8_varlen(L, o=0x4008) == -3
     assert _fp8_varlen(L, mq=0) == 0                   # no query rows: a no-op

@@ -98,7 +98,7 @@ def _check_heads(prep, o, lse, B, H, S, scale, causal, rows=None):
     return stats
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S", [128, 600])
 def test_fp8_attention_elementwise(D, causal, S):

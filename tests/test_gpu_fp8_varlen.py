@@ -105,7 +105,7 @@ def test_varlen_blocks_and_prep_parity(D):
             start += n
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_varlen_attention_elementwise(D, causal):
     H = 2
