@@ -405,7 +405,8 @@ def main(argv=None):
         def hot_path(i_, o_, st):
             return [lambda: api.fa_bwd(*i_, *o_, w.B, w.H, Sq, Sk, w.D, scale, w.causal, workspace=bwd_ws,
                                        workspace_bytes=ws_bytes, stream=st)]
-        names = ["fa_bwd (bwd_prep_kernel + fa_bwd_kernel dK/dV + fa_bwd_kernel dQ)"]
+        names = ["fa_bwd (bwd_prep_kernel + fa_bwd_kernel dK/dV + fa_bwd_kernel dQ)" if w.D <= 128 else
+                 "fa_bwd (bwd_prep_kernel + fa_bwd_kernel dV + fa_bwd_kernel dK + fa_bwd_kernel dQ)"]
     elif w.page_size:
         kc, vc, table, seqlens = (inputs[n] for n in ("k_cache", "v_cache", "block_table", "seqlens_k"))
         max_pages = table.shape[1]
@@ -590,7 +591,8 @@ def main(argv=None):
                          "paged K/V cache stays resident" if w.page_size else
                          "pinned host -> device copy of Q, K, V and device -> host copy of O, LSE every step")
                         + "; copies of neighbouring steps overlap compute (two buffer sets, H2D / D2H streams)"},
-        "gpu_launches": args.steps * (3 if w.backward else 2 if (w.splitkv or (w.page_size and w.Sq == 1))
+        "gpu_launches": args.steps * ((4 if w.D == 256 else 3) if w.backward
+                                      else 2 if (w.splitkv or (w.page_size and w.Sq == 1))
                                       else len(kernels)),
         "clocks": clk.summary(),
     }

@@ -23,6 +23,15 @@
 // The dQ kernel recomputes S and dP (7 instead of 5 matrix products in all)
 // so that every output row is written by exactly one CTA.
 //
+// D = 256: the accumulators of dK and dV (256 tensor-memory columns each) and
+// the two 128-column score buffers do not fit the 512 columns together, nor do
+// two resident and two streamed tiles of 64 KB fit shared memory. The
+// gradient then takes three kernels -- dQ, dK, dV -- and the streamed tiles
+// arrive as two 128-column halves (32 KB ring slots); the streamed operand
+// that the accumulating product needs again (K for dQ, Q for dK) is loaded a
+// second time from L2 rather than held. dK recomputes S^T and dP^T, dV
+// recomputes S^T: 8 products run where 5 are algorithmic.
+//
 // Roles: eight "softmax" warps (two warpgroups, each owning half of the 128
 // streamed columns of every resident row: thread = resident row), one MMA
 // warp (one thread issues), one load warp (TMA). The softmax warps hand a
@@ -41,16 +50,27 @@
 
 namespace fa {
 
-template <int D_, int STAGES_, int KIND_, bool DQ_>
+// What one backward kernel computes: dQ (resident Q, dO), dK and dV together
+// (resident K, V; D <= 128), or, at D = 256, dK alone or dV alone.
+enum BwdMode : int { kBwdDQ = 0, kBwdDKDV = 1, kBwdDK = 2, kBwdDV = 3 };
+
+template <int D_, int STAGES_, int KIND_, int MODE_>
 struct BwdCfg {
   static constexpr int D = D_;
   static constexpr int STAGES = STAGES_;
   static constexpr int KIND = KIND_;
-  static constexpr bool DQ = DQ_;
+  static constexpr int MODE = MODE_;
+  static constexpr bool DQ = MODE == kBwdDQ;   // resident Q, dO; streamed K, V
+  // D = 256: streamed tiles in two 128-column halves, one ring slot each
+  static constexpr bool kSplit = D == 256;
+  static constexpr bool kNeedY = MODE != kBwdDV;    // dP (dP^T) and dS (dS^T) are made
+  static constexpr bool kStoreP = MODE == kBwdDKDV || MODE == kBwdDV;   // P^T kept for dV += P^T dO
+  static constexpr int kResident = MODE == kBwdDV ? 1 : 2;              // R1 (and R2) held
   static constexpr int kBoxCols = 64;               // 16-bit elements per 128-byte box row
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kBoxBytes = 128 * 128;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;   // one 128-row tile
+  static constexpr int kTBytes = kSplit ? 2 * kBoxBytes : kTileBytes;   // one streamed ring slot
   static constexpr int kKSteps = D / 16;                 // MMA K steps over D
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kMmaWarp = 8, kLoadWarp = 9;
@@ -58,13 +78,13 @@ struct BwdCfg {
   static constexpr int kTmemCols = 512;
   // tensor memory: accumulators at 0 (dQ, or dV) and D (dK); X (S or S^T)
   // at 256 and Y (dP or dP^T) at 384; the 16-bit P / dS go over X / Y
-  static constexpr uint32_t kColAcc1 = DQ ? 0u : (uint32_t)D;   // dQ or dK
+  static constexpr uint32_t kColAcc1 = MODE == kBwdDKDV ? (uint32_t)D : 0u;   // dQ or dK
   static constexpr uint32_t kColAcc2 = 0u;                      // dV
   static constexpr uint32_t kColX = 256u, kColY = 384u;
   // shared memory
   static constexpr int kOffR = 0;                                // R1, R2
-  static constexpr int kOffT = 2 * kTileBytes;                   // ring of T tiles
-  static constexpr int kOffVec = kOffT + STAGES * kTileBytes;    // per-warp column constants
+  static constexpr int kOffT = kResident * kTileBytes;           // ring of T tiles (halves at D = 256)
+  static constexpr int kOffVec = kOffT + STAGES * kTBytes;       // per-warp column constants
   static constexpr int kVecBytes = DQ ? 0 : 2 * 64 * 4;
   static constexpr int kOffBar = kOffVec + kSoftmaxWarps * kVecBytes;
   static constexpr int kTileRing = 4;
@@ -81,9 +101,10 @@ struct BwdCfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 4 * kTileRing + 1024;
 
-  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(D == 64 || D == 128 || D == 256, "head dimension");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(2 * D <= 256, "accumulators below the score columns");
+  static_assert(kSplit ? MODE != kBwdDKDV : (MODE == kBwdDQ || MODE == kBwdDKDV), "modes per head size");
+  static_assert((MODE == kBwdDKDV ? 2 * D : D) <= 256, "accumulators below the score columns");
 };
 
 // Work tile: one 128-row block of the resident side of one (sequence, head).
@@ -174,14 +195,28 @@ __device__ void bwd_load_role(const CUtensorMap* tr1, const CUtensorMap* tr2, co
     for (int bx = 0; bx < C::kBoxes; ++bx)
       ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + bx * C::kBoxCols, row, b);
   };
-  auto load_t = [&](const CUtensorMap* m, int h, int row) -> bool {
+  // one streamed ring slot: a whole tile, or (D = 256) its 128-column half
+  auto load_t = [&](const CUtensorMap* m, int h, int row, int half) -> bool {
     const int s = tc % C::STAGES;
     const uint32_t ph = (tc / C::STAGES) & 1u;
     if (!wt.wait(bar(C::kBarTEmpty + s), ph ^ 1u, 22)) return false;
-    ptx::mbar_arrive_expect_tx(bar(C::kBarTFull + s), C::kTileBytes);
-    load_tile(m, h, row, sbase + C::kOffT + s * C::kTileBytes, bar(C::kBarTFull + s));
+    ptx::mbar_arrive_expect_tx(bar(C::kBarTFull + s), C::kTBytes);
+    const uint32_t dst = sbase + C::kOffT + s * C::kTBytes;
+    if (C::kSplit) {
+#pragma unroll
+      for (int bx = 0; bx < 2; ++bx)
+        ptx::tma_load_2d(dst + bx * C::kBoxBytes, m, h * C::D + 128 * half + bx * C::kBoxCols, row,
+                         bar(C::kBarTFull + s));
+    } else {
+      load_tile(m, h, row, dst, bar(C::kBarTFull + s));
+    }
     ++tc;
     return true;
+  };
+  // a streamed block: one slot, or (D = 256) two consecutive half slots
+  auto load_block = [&](const CUtensorMap* m, int h, int row) -> bool {
+    if (!load_t(m, h, row, 0)) return false;
+    return !C::kSplit || load_t(m, h, row, 1);
   };
 
   for (int j = 0; ok; ++j) {
@@ -194,13 +229,31 @@ __device__ void bwd_load_role(const CUtensorMap* tr1, const CUtensorMap* tr2, co
     const BwdTile ti = bwd_tile<C::DQ, CAUSAL>(p, w);
     if (!ti.live || ti.n_t == 0) continue;
     if (!wt.wait(bar(C::kBarREmpty), (rcount & 1u) ^ 1u, 21)) break;
-    ptx::mbar_arrive_expect_tx(bar(C::kBarRFull), 2 * C::kTileBytes);
+    ptx::mbar_arrive_expect_tx(bar(C::kBarRFull), C::kResident * C::kTileBytes);
     load_tile(tr1, ti.h, ti.rtok + ti.r0, sbase + C::kOffR, bar(C::kBarRFull));
-    load_tile(tr2, ti.h, ti.rtok + ti.r0, sbase + C::kOffR + C::kTileBytes, bar(C::kBarRFull));
+    if (C::kResident == 2) load_tile(tr2, ti.h, ti.rtok + ti.r0, sbase + C::kOffR + C::kTileBytes, bar(C::kBarRFull));
     ++rcount;
-    for (int i = 0; ok && i < ti.n_t; ++i) {
-      const int row = ti.ttok + 128 * (ti.t_first + i);
-      ok = load_t(tt1, ti.h, row) && load_t(tt2, ti.h, row);
+    const int n = ti.n_t;
+    auto trow = [&](int i) { return ti.ttok + 128 * (ti.t_first + i); };
+    if (!C::kSplit) {
+      // T1, T2 of each block, in the order the MMA thread consumes them
+      for (int i = 0; ok && i < n; ++i) ok = load_block(tt1, ti.h, trow(i)) && load_block(tt2, ti.h, trow(i));
+    } else if (C::kNeedY) {
+      // dQ, dK at D = 256: T1_0, T2_0, then per block i: T1_{i+1}, T1_i again
+      // (for the accumulating product), T2_{i+1}
+      ok = load_block(tt1, ti.h, trow(0)) && load_block(tt2, ti.h, trow(0));
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n) ok = load_block(tt1, ti.h, trow(i + 1));
+        ok = ok && load_block(tt1, ti.h, trow(i));
+        if (ok && i + 1 < n) ok = load_block(tt2, ti.h, trow(i + 1));
+      }
+    } else {
+      // dV at D = 256: T1_0, then per block i: T2_i, T1_{i+1}
+      ok = load_block(tt1, ti.h, trow(0));
+      for (int i = 0; ok && i < n; ++i) {
+        ok = load_block(tt2, ti.h, trow(i));
+        if (ok && i + 1 < n) ok = load_block(tt1, ti.h, trow(i + 1));
+      }
     }
   }
   if (*wt.abort_flag) {
@@ -221,7 +274,7 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
   constexpr uint32_t idesc_s = ptx::make_idesc(fmt, false, 128, 128);   // X, Y: 128 x 128
   constexpr uint32_t idesc_acc = ptx::make_idesc(fmt, true, 128, C::D); // acc += Z T (T MN-major)
   const uint32_t r1 = sbase + C::kOffR, r2 = r1 + C::kTileBytes;
-  auto slot_addr = [&](uint32_t c) { return sbase + C::kOffT + (c % C::STAGES) * C::kTileBytes; };
+  auto slot_addr = [&](uint32_t c) { return sbase + C::kOffT + (c % C::STAGES) * C::kTBytes; };
 
   // X or Y = R T^T over the head dimension (both K-major), committed to `b`
   auto mm_s = [&](uint32_t col, uint32_t r_addr, uint32_t t_addr, int b) {
@@ -249,6 +302,36 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
     ptx::tc_fence_after();
     return r;
   };
+  // D = 256, T in two half slots c, c + 1:
+  // X or Y = R T^T over the 256 columns (steps 0-7 from half 0, 8-15 from half 1)
+  auto mm_s_split = [&](uint32_t col, uint32_t r_addr, uint32_t c, int b) {
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t r_off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+      const uint32_t t_off = ((kk >> 2) & 1) * C::kBoxBytes + (kk & 3) * 32;
+      ptx::mma_f16_ss(tmem + col, ptx::smem_desc_sw128(r_addr + r_off, 16, 1024),
+                      ptx::smem_desc_sw128(slot_addr(c + (kk >> 3)) + t_off, 16, 1024), idesc_s, kk > 0);
+    }
+    ptx::mma_commit(bar(b));
+  };
+  // acc (+)= Z T over 256 columns: accumulator half h from T's half slot c + h
+  constexpr uint32_t idesc_half = ptx::make_idesc(fmt, true, 128, 128);
+  auto mm_acc_split = [&](uint32_t acc_col, uint32_t z_col, uint32_t c, bool acc) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t zc = z_col + 64u * (kk >> 2) + 8u * (kk & 3);
+        const uint64_t b = ptx::smem_desc_sw128(slot_addr(c + half) + kk * 16 * 128, C::kBoxBytes, 1024);
+        ptx::mma_f16_ts(tmem + acc_col + 128u * half, tmem + zc, b, idesc_half, (acc || kk > 0) ? 1u : 0u);
+      }
+    }
+  };
+  auto halves_ready = [&](uint32_t c) { return t_ready(c) && t_ready(c + 1); };
+  auto release_halves = [&](uint32_t c) {
+    ptx::mma_commit(bar(C::kBarTEmpty + (int)(c % C::STAGES)));
+    ptx::mma_commit(bar(C::kBarTEmpty + (int)((c + 1) % C::STAGES)));
+  };
 
   // Issue order per block i (T tiles of block i in slots c, c + 1):
   //   [P_i handed back]  dV += P_i^T dO_i (dK/dV kernel),  X_{i+1}
@@ -267,6 +350,66 @@ __device__ void bwd_mma_role(const BwdParams& p, uint32_t sbase, uint32_t tmem, 
     ++rcount;
     ptx::tc_fence_after();
     const int n = ti.n_t;
+    if (C::kSplit) {
+      // D = 256: the same overlap of the next block's scores with this
+      // block's softmax work, T in half slots; each pair of half slots is
+      // released as soon as its products have read it
+      uint32_t c = tc;
+      if (!(ok = halves_ready(c))) break;
+      mm_s_split(C::kColX, r1, c, C::kBarXFull);
+      release_halves(c);
+      c += 2;
+      if (C::kNeedY) {
+        if (!(ok = halves_ready(c))) break;
+        mm_s_split(C::kColY, r2, c, C::kBarYFull);
+        release_halves(c);
+        c += 2;
+      }
+      if (n == 1) ptx::mma_commit(bar(C::kBarREmpty));   // last use of R1, R2
+      for (int i = 0; i < n; ++i, ++it) {
+        const bool more = i + 1 < n;
+        if (!(ok = wt.wait(bar(C::kBarPFull), it & 1u, 25))) break;
+        ptx::tc_fence_after();
+        if (!C::kNeedY) {
+          // dV: dV += P^T dO, then the next block's S^T over P^T
+          if (!(ok = halves_ready(c))) break;
+          mm_acc_split(C::kColAcc2, C::kColX, c, i > 0);
+          release_halves(c);
+          c += 2;
+          if (more) {
+            if (!(ok = halves_ready(c))) break;
+            mm_s_split(C::kColX, r1, c, C::kBarXFull);
+            release_halves(c);
+            c += 2;
+            if (i + 2 == n) ptx::mma_commit(bar(C::kBarREmpty));
+          }
+          continue;
+        }
+        if (more) {
+          if (!(ok = halves_ready(c))) break;
+          mm_s_split(C::kColX, r1, c, C::kBarXFull);
+          release_halves(c);
+          c += 2;
+        }
+        if (!(ok = wt.wait(bar(C::kBarDSFull), it & 1u, 26))) break;
+        ptx::tc_fence_after();
+        if (!(ok = halves_ready(c))) break;
+        mm_acc_split(C::kColAcc1, C::kColY, c, i > 0);   // dQ += dS K  or  dK += dS^T Q
+        release_halves(c);
+        c += 2;
+        if (more) {
+          if (!(ok = halves_ready(c))) break;
+          mm_s_split(C::kColY, r2, c, C::kBarYFull);
+          release_halves(c);
+          c += 2;
+          if (i + 2 == n) ptx::mma_commit(bar(C::kBarREmpty));
+        }
+      }
+      if (!ok) break;
+      tc = c;
+      ptx::mma_commit(bar(C::kBarAccFull));
+      continue;
+    }
     if (!(ok = t_ready(tc))) break;
     mm_s(C::kColX, r1, slot_addr(tc), C::kBarXFull);
     if (!(ok = t_ready(tc + 1))) break;
@@ -356,14 +499,15 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
     const int row = ti.r0 + r;                         // resident row within the sequence
     const bool row_ok = row < (C::DQ ? ti.Lq : ti.Lk);
     const int64_t tok = (int64_t)ti.rtok + row;
-    uint16_t* out1 = reinterpret_cast<uint16_t*>(p.dr1) + (tok * p.H + ti.h) * C::D;
-    uint16_t* out2 = C::DQ ? nullptr : reinterpret_cast<uint16_t*>(p.dr2) + (tok * p.H + ti.h) * C::D;
+    // dr1: dQ or dK (every mode but dV alone); dr2: dV (dK/dV and dV alone)
+    uint16_t* out1 = C::MODE != kBwdDV ? reinterpret_cast<uint16_t*>(p.dr1) + (tok * p.H + ti.h) * C::D : nullptr;
+    uint16_t* out2 = C::kStoreP ? reinterpret_cast<uint16_t*>(p.dr2) + (tok * p.H + ti.h) * C::D : nullptr;
     if (ti.n_t == 0) {
       // no pair of this block is visible: zero gradient rows
-      if (C::DQ) {
-        zero_row<C::KIND>(out1 + g * (C::D / 2), C::D / 2, row_ok);
-      } else {
+      if (C::MODE == kBwdDKDV) {
         zero_row<C::KIND>(g == 0 ? out1 : out2, C::D, row_ok);
+      } else {
+        zero_row<C::KIND>((C::MODE == kBwdDV ? out2 : out1) + g * (C::D / 2), C::D / 2, row_ok);
       }
       continue;
     }
@@ -446,17 +590,18 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
           pv[32 * ch + j] = p0;
           pv[32 * ch + j + 1] = p1;
         }
-        if (!C::DQ) {
+        if (C::kStoreP) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) pk[j] = pack16<C::KIND>(pv[32 * ch + 2 * j], pv[32 * ch + 2 * j + 1]);
           ptx::tmem_st16(tl + C::kColX + 64 * g + 16 * ch, pk);
         }
       }
-      if (!C::DQ) ptx::tmem_wait_st();
+      if (C::kStoreP) ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull));
+      if (!C::kNeedY) continue;   // dV alone: no dP, no dS
       // phase 2: dS = P (dP - Delta), 16-bit, over dP (columns 64 g .. 64 g + 31)
       if (!(ok = wt.wait_warp(bar(C::kBarYFull), it & 1u, 28))) break;
       ptx::tc_fence_after();
@@ -493,12 +638,16 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
     if (!wt.wait_warp(bar(C::kBarAccFull), acount & 1u, 29)) return;
     ++acount;
     ptx::tc_fence_after();
-    if (C::DQ) {
-      store_acc_row<C::KIND>(tl + C::kColAcc1 + g * (C::D / 2), C::D / 2, p.scale, out1 + g * (C::D / 2), row_ok);
-    } else if (g == 0) {
-      store_acc_row<C::KIND>(tl + C::kColAcc1, C::D, p.scale, out1, row_ok);   // dK
+    if (C::MODE == kBwdDKDV) {
+      if (g == 0)
+        store_acc_row<C::KIND>(tl + C::kColAcc1, C::D, p.scale, out1, row_ok);   // dK
+      else
+        store_acc_row<C::KIND>(tl + C::kColAcc2, C::D, 1.f, out2, row_ok);       // dV
+    } else if (C::MODE == kBwdDV) {
+      // each warpgroup writes half of the row
+      store_acc_row<C::KIND>(tl + C::kColAcc2 + g * (C::D / 2), C::D / 2, 1.f, out2 + g * (C::D / 2), row_ok);
     } else {
-      store_acc_row<C::KIND>(tl + C::kColAcc2, C::D, 1.f, out2, row_ok);       // dV
+      store_acc_row<C::KIND>(tl + C::kColAcc1 + g * (C::D / 2), C::D / 2, p.scale, out1 + g * (C::D / 2), row_ok);
     }
     // the next tile's first accumulating MMAs overwrite these columns only
     // after this warp's next P and dS hand-offs
@@ -507,12 +656,12 @@ __device__ void bwd_softmax_role(const BwdParams& p, uint32_t sbase, uint8_t* sm
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int STAGES, int KIND, bool DQ, bool CAUSAL>
+template <int D, int STAGES, int KIND, int MODE, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tr1, const __grid_constant__ CUtensorMap tr2,
                   const __grid_constant__ CUtensorMap tt1, const __grid_constant__ CUtensorMap tt2,
                   const BwdParams p) {
-  using C = BwdCfg<D, STAGES, KIND, DQ>;
+  using C = BwdCfg<D, STAGES, KIND, MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -572,10 +721,10 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, int STAGES, int KIND, bool DQ>
+template <int D, int STAGES, int KIND, int MODE>
 cudaError_t launch_bwd_dir(const BwdLaunch& L) {
-  using C = BwdCfg<D, STAGES, KIND, DQ>;
-  auto kern = L.causal ? fa_bwd_kernel<D, STAGES, KIND, DQ, true> : fa_bwd_kernel<D, STAGES, KIND, DQ, false>;
+  using C = BwdCfg<D, STAGES, KIND, MODE>;
+  auto kern = L.causal ? fa_bwd_kernel<D, STAGES, KIND, MODE, true> : fa_bwd_kernel<D, STAGES, KIND, MODE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = L.p.ntiles < L.num_sms ? L.p.ntiles : L.num_sms;
@@ -587,8 +736,8 @@ cudaError_t launch_bwd_dir(const BwdLaunch& L) {
 template <int D, int STAGES_KV, int STAGES_Q>
 cudaError_t launch_bwd_impl(const BwdLaunch& L) {
   if (L.kind == kF16)
-    return L.dq ? launch_bwd_dir<D, STAGES_Q, kF16, true>(L) : launch_bwd_dir<D, STAGES_KV, kF16, false>(L);
-  return L.dq ? launch_bwd_dir<D, STAGES_Q, kBF16, true>(L) : launch_bwd_dir<D, STAGES_KV, kBF16, false>(L);
+    return L.dq ? launch_bwd_dir<D, STAGES_Q, kF16, kBwdDQ>(L) : launch_bwd_dir<D, STAGES_KV, kF16, kBwdDKDV>(L);
+  return L.dq ? launch_bwd_dir<D, STAGES_Q, kBF16, kBwdDQ>(L) : launch_bwd_dir<D, STAGES_KV, kBF16, kBwdDKDV>(L);
 }
 
 }  // namespace fa

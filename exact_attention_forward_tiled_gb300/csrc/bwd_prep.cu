@@ -66,6 +66,8 @@ cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, f
     bwd_prep_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(po, pd, lse, lse2, delta, total_q, H, Sq, lse_varlen, fp16);
   else if (D == 128)
     bwd_prep_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(po, pd, lse, lse2, delta, total_q, H, Sq, lse_varlen, fp16);
+  else if (D == 256)
+    bwd_prep_kernel<256><<<(unsigned)blocks, 256, 0, stream>>>(po, pd, lse, lse2, delta, total_q, H, Sq, lse_varlen, fp16);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -719,7 +719,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   // ---- host-side argument checks (no device access)
   if (dtype == FA_FP8_E4M3) return FA_ERR_UNSUPPORTED;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (B < 0 || H <= 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -761,16 +761,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if ((st = make_map(&mk, k, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
   if ((st = make_map(&mv, v, dt, 2, cols, (uint64_t)Tk, 64, 128)) != FA_OK) return st;
   if ((st = make_map(&mdo, dout, dt, 2, cols, (uint64_t)Tq, 64, 128)) != FA_OK) return st;
-  for (int dir = 0; dir < 2; ++dir) {   // 0: dK, dV;  1: dQ
+  // launches: dK and dV together, then dQ; at D = 256 (their accumulators do
+  // not fit tensor memory together) dV, dK, then dQ
+  const int n_dir = D == 256 ? 3 : 2;
+  for (int dir = 0; dir < n_dir; ++dir) {
     fa::BwdLaunch L;
     std::memset(&L, 0, sizeof(L));
-    const bool dqk = dir == 1;
+    const bool dqk = dir == n_dir - 1;
+    L.part = D == 256 && !dqk ? (dir == 0 ? 2 : 1) : 0;
     L.tr1 = dqk ? mq : mk;
     L.tr2 = dqk ? mdo : mv;
     L.tt1 = dqk ? mk : mq;
     L.tt2 = dqk ? mv : mdo;
-    L.p.dr1 = dqk ? dq : dk;
-    L.p.dr2 = dqk ? nullptr : dv;
+    L.p.dr1 = dqk ? dq : (L.part == 2 ? nullptr : dk);
+    L.p.dr2 = dqk || L.part == 1 ? nullptr : dv;
     L.p.lse2 = lse2;
     L.p.delta = delta;
     L.p.cu_q = cu_seqlens_q;
@@ -796,7 +800,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (L.p.ntiles == 0) continue;
     SlotHold hold(dev, s);
     if ((L.p.sched = hold.sched()) == nullptr) return FA_ERR_BUSY;
-    const cudaError_t e = D == 64 ? fa::launch_bwd_d64(L) : fa::launch_bwd_d128(L);
+    const cudaError_t e = D == 64 ? fa::launch_bwd_d64(L) : D == 128 ? fa::launch_bwd_d128(L) : fa::launch_bwd_d256(L);
     hold.launched(e == cudaSuccess);
     if (e != cudaSuccess) {
       cudaGetLastError();

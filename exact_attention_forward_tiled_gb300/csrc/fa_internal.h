@@ -150,12 +150,14 @@ struct BwdLaunch {
   int kind;  // kF16 or kBF16
   bool causal;
   bool dq;   // true: dQ kernel, false: dK/dV kernel
+  int part;  // D = 256 dK/dV side, one kernel each: 1 dK, 2 dV (0 below D = 256: both)
   int num_sms;
   cudaStream_t stream;
 };
 
 cudaError_t launch_bwd_d64(const BwdLaunch& L);
 cudaError_t launch_bwd_d128(const BwdLaunch& L);
+cudaError_t launch_bwd_d256(const BwdLaunch& L);
 // lse2 / delta of every (query token, head) from O, dO and the forward's LSE
 // (lse_varlen: LSE is [H, total_q], else [B, H, Sq])
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* delta,

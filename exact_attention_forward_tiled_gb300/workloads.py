@@ -60,6 +60,8 @@ WORKLOADS = {
                    note="bf16 backward B=4 H=16 Sq=Sk=8192 D=128 non-causal"),
     "b2": Workload("bf16_bwd_causal_B2_H16_S16384_D128", "bf16", 2, 16, 16384, 16384, 128, True, 8,
                    backward=True, note="bf16 backward causal B=2 H=16 Sq=Sk=16384 D=128"),
+    "b3": Workload("bf16_bwd_causal_B1_H8_S16384_D256", "bf16", 1, 8, 16384, 16384, 256, True, 11,
+                   backward=True, note="bf16 backward causal B=1 H=8 Sq=Sk=16384 D=256 (the c3b shape)"),
     # paged K/V: Sq new queries per sequence at the end of an Sk-key context
     # whose keys sit in shuffled 16-key pages
     "p1": Workload("bf16_paged_prefill_B8_H16_Sq1024_Sk8192_D128_page16", "bf16", 8, 16, 1024, 8192, 128, True, 9,

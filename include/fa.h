@@ -330,15 +330,17 @@ size_t fa_bwd_workspace_size(int H, int total_q);
  *   lse          the forward's LSE (fp32, [B, H, Sq] or varlen [H, total_q])
  *   dq, dk, dv   outputs, shapes and type of q, k, v (written; every row of
  *                every sequence, 0 where no pair is visible)
- *   B..dtype     as fa_fwd; D = 64 or 128 (256 -> FA_ERR_UNSUPPORTED)
+ *   B..dtype     as fa_fwd; D = 64, 128 or 256
  *   workspace    device scratch of at least fa_bwd_workspace_size(H, total_q)
  *                bytes, 256-byte aligned; holds the per-row constants
  *
  * P and dS are rounded to the input type before they enter the tensor-core
  * products (as P is in the forward); accumulation is fp32. Deterministic: no
  * atomics, every output row is written by one CTA. Three kernels on `stream`
- * (row constants, dK/dV, dQ). Bad varlen sequences are skipped and reported
- * as FA_ERR_DEVICE_SEQLENS by fa_get_device_status.
+ * (row constants, dK/dV, dQ), four at D = 256 (row constants, dV, dK, dQ:
+ * the dK and dV accumulators do not fit tensor memory together). Bad varlen
+ * sequences are skipped and reported as FA_ERR_DEVICE_SEQLENS by
+ * fa_get_device_status.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D,

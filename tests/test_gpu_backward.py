@@ -129,27 +129,28 @@ def _check(B, H, Sq, Sk, D, causal, dtype, seed, lq=None, lk=None):
     return dq, dk, dv, worst
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Sq,Sk", [(128, 128), (300, 300), (256, 700), (700, 256), (1, 513), (129, 1)])
 def test_backward_matches_oracle(D, causal, Sq, Sk):
     _check(2, 2, Sq, Sk, D, causal, torch.bfloat16, seed=Sq + 7 * Sk + D + causal)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_backward_fp16(D):
     _check(1, 3, 333, 520, D, True, torch.float16, seed=77 + D)
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_backward_varlen(causal, D):
     _check(0, 2, 0, 0, D, causal, torch.bfloat16, seed=90 + D + causal, lq=[1, 300, 128, 0, 257, 40],
            lk=[129, 5, 400, 64, 0, 40])
 
 
-def test_backward_is_deterministic():
-    B, H, S, D = 2, 4, 640, 128
+@pytest.mark.parametrize("D", [128, 256])
+def test_backward_is_deterministic(D):
+    B, H, S = 2, 4, 640
     q, k, v, do = (_rand((B * S, H, D), torch.bfloat16, 200 + i) for i in range(4))
     o, lse = api.attention_forward(q, k, v, causal=True, batch=B)
     g1 = api.attention_backward(q, k, v, o, lse, do, causal=True, batch=B)
