@@ -90,6 +90,13 @@ struct FwdCfg {
   // warp) gives its registers to the two softmax warpgroups: 384 threads
   // launch at 168 registers each (64512); 128 x 64 + 256 x 216 = 63488 <= 64512.
   static constexpr bool kRebalance = QT == 2;
+  // QT = 2, 16-bit: softmax warpgroup 1 frees the K/V ring slots when it sees
+  // S1 (K of the block and V of the one before have been read by then), which
+  // takes two commits per block off the MMA thread (a commit costs it about
+  // as much as a product): c2 1456 -> 1491 TFLOP/s, same box. The e4m3
+  // kernel, whose softmax is the critical path, keeps the commits (1650
+  // against 1632 with the softmax release).
+  static constexpr bool kSoftmaxFreesKV = QT == 2 && !kFp8;
   static constexpr int kRegsLow = 64, kRegsHigh = 216;
   static constexpr int kThreads = kRebalance ? 384 : 32 * (kSoftmaxWarps + 3);
   static_assert(!kRebalance || kThreads * 168 >= 128 * kRegsLow + 256 * kRegsHigh, "register split");
@@ -491,11 +498,11 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
         const uint32_t ck = kvc + 2 * i, cv = ck + 1;
         if (i > 0) {
           if (!(ok = pv(C::col_o(1), C::col_s(1), slot_addr(cv - 2), i - 1 > 0, 1, (it + i - 1) & 1u))) break;
-          ptx::mma_commit(bar(C::kBarKVEmpty + slot(cv - 2)));
+          if (!C::kSoftmaxFreesKV) ptx::mma_commit(bar(C::kBarKVEmpty + slot(cv - 2)));
         }
         qk(C::col_s(1), sq + C::kTileBytes, slot_addr(ck));
         ptx::mma_commit(bar(C::kBarSFull + 1));
-        ptx::mma_commit(bar(C::kBarKVEmpty + slot(ck)));
+        if (!C::kSoftmaxFreesKV) ptx::mma_commit(bar(C::kBarKVEmpty + slot(ck)));
         if (i == n - 1) ptx::mma_commit(bar(C::kBarQEmpty + 1));   // last use of Q1
         if (!(ok = kv_ready(cv))) break;
         if (!(ok = pv(C::col_o(0), C::col_s(0), slot_addr(cv), i > 0, 0, (it + i) & 1u))) break;
@@ -510,7 +517,7 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
       if (!ok) break;
       const uint32_t cl = kvc + 2 * n - 1;
       if (!(ok = pv(C::col_o(1), C::col_s(1), slot_addr(cl), n - 1 > 0, 1, (it + n - 1) & 1u))) break;
-      ptx::mma_commit(bar(C::kBarKVEmpty + slot(cl)));
+      if (!C::kSoftmaxFreesKV) ptx::mma_commit(bar(C::kBarKVEmpty + slot(cl)));
       ptx::mma_commit(bar(C::kBarOFull + 1));
       kvc += 2 * n;
       it += n;
@@ -652,6 +659,14 @@ __device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t
       const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
       if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;
       ptx::tc_fence_after();
+      if (C::kSoftmaxFreesKV && t == 1 && quarter == 0 && lane == 0) {
+        // S1 of block `it` proves QK0, QK1 of the block and the PV1 before
+        // them done (one thread's products complete in order): K of this
+        // block and V of the previous one (it - 1, possibly of the previous
+        // work tile) have been read; their ring slots are free
+        ptx::mbar_arrive(bar(C::kBarKVEmpty + (int)((2u * it) % C::STAGES)));
+        if (it > 0) ptx::mbar_arrive(bar(C::kBarKVEmpty + (int)((2u * it - 1u) % C::STAGES)));
+      }
       const uint32_t s_addr = tl + C::col_s(buf);
       uint32_t sv[128];
 #pragma unroll
