@@ -20,8 +20,9 @@ __device__ int g_fa_status;
 // Tile-scheduler counters {next tile, CTAs done}, one pair per launch slot.
 // A launch takes a free slot (fa::SlotTable: never used, or its last launch
 // has finished, which an event recorded after that launch tells); its last
-// CTA puts the pair back to zero. Up to kSchedSlots launches may be in flight
-// on one device at the same time; one more is refused with FA_ERR_BUSY.
+// CTA puts the pair back to zero. With kSchedSlots launches in flight on one
+// device, the next one reuses the slot handed out longest ago and its stream
+// waits for that slot's event first (SlotHold).
 constexpr int kSchedSlots = 64;
 __device__ unsigned int g_fa_sched[kSchedSlots][2];
 
@@ -91,12 +92,19 @@ int current_device(DevInfo** out) {
   return FA_OK;
 }
 
-// One persistent launch's hold on a scheduler slot: the constructor takes a
-// free slot (sched == nullptr: all kSchedSlots held by launches in flight),
-// launched() records the slot's event after the launch went out. On a stream
-// that is being captured into a graph no event is recorded or queried (the
-// library does not see the graph's replays; the slot is handed out as free
-// again, and replays must not overlap other launches of the library).
+// One persistent launch's hold on a scheduler slot, taken under the
+// device's slot lock for the whole launch:
+//   - a free slot is used as it is;
+//   - when all kSchedSlots are held by launches in flight, the slot handed
+//     out longest ago is reused and the stream first waits for its event
+//     (cudaStreamWaitEvent: the GPU orders the two launches, the host does
+//     not block);
+//   - launched() records the slot's event after the launch went out.
+// On a stream that is being captured into a graph no event is queried,
+// waited for or recorded (a capture may not touch events from outside it,
+// and the library does not see the graph's replays): the launch gets the
+// next slot in turn, untracked, and replays must not overlap other launches
+// of the library. sched() == nullptr: the stream wait could not be issued.
 class SlotHold {
  public:
   SlotHold(DevInfo* dev, cudaStream_t stream) : dev_(dev), stream_(stream), lock_(dev->slot_mu) {
@@ -106,22 +114,33 @@ class SlotHold {
       cs = cudaStreamCaptureStatusActive;
     }
     capturing_ = cs != cudaStreamCaptureStatusNone;
-    slot_ = dev->slots.take([dev](int i) {
-      const cudaError_t q = cudaEventQuery(dev->done_ev[i]);
-      if (q == cudaErrorNotReady) return false;
-      if (q != cudaSuccess) cudaGetLastError();
-      return true;
-    });
-    if (slot_ >= 0 && capturing_) dev->slots.release(slot_);
+    if (capturing_) {
+      slot_ = dev->slots.untracked();
+      return;
+    }
+    slot_ = dev->slots.take(
+        [dev](int i) {
+          const cudaError_t q = cudaEventQuery(dev->done_ev[i]);
+          if (q == cudaErrorNotReady) return false;
+          if (q != cudaSuccess) cudaGetLastError();
+          return true;
+        },
+        reused_);
+    if (reused_ && cudaStreamWaitEvent(stream, dev->done_ev[slot_], 0) != cudaSuccess) {
+      cudaGetLastError();
+      slot_ = -1;   // still held by its previous launch
+    }
   }
   unsigned int* sched() const { return slot_ < 0 ? nullptr : dev_->sched + 2 * slot_; }
   // the launch went out (ok) or failed
   void launched(bool ok) {
     if (slot_ < 0 || capturing_) return;
-    if (!ok || cudaEventRecord(dev_->done_ev[slot_], stream_) != cudaSuccess) {
-      cudaGetLastError();
-      if (!ok) dev_->slots.release(slot_);
+    if (!ok) {
+      // a reused slot stays held by its previous launch, whose event stands
+      if (!reused_) dev_->slots.release(slot_);
+      return;
     }
+    if (cudaEventRecord(dev_->done_ev[slot_], stream_) != cudaSuccess) cudaGetLastError();
   }
 
  private:
@@ -129,6 +148,7 @@ class SlotHold {
   cudaStream_t stream_;
   std::lock_guard<std::mutex> lock_;
   bool capturing_ = false;
+  bool reused_ = false;
   int slot_ = -1;
 };
 
@@ -203,7 +223,7 @@ const char* fa_strerror(int s) {
     case FA_ERR_DEVICE_SEQLENS: return "cu_seqlens entry out of bounds; sequence skipped";
     case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
     case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in 64 MiB array holds";
-    case FA_ERR_BUSY: return "all 64 scheduler slots of the device are held by launches still in flight";
+    case FA_ERR_BUSY: return "no scheduler slot could be given to the launch (the stream could not wait for one)";
     default: return "unknown status";
   }
 }

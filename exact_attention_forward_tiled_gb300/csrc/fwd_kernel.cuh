@@ -641,20 +641,35 @@ __device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t
         vs_row = p.v_scale + hb * p.nblk_k;
       }
       c_q = p.c * __ldg(qs_row + (int64_t)min(ti.qblk * C::QT + t, nq - 1) * sstride);
+      // v_ref = the head's largest V block scale: the lanes of the warp take
+      // every 32nd block, then a butterfly max
       float vmax = 0.f;
-      for (int j = 0; j < nk; ++j) vmax = fmaxf(vmax, __ldg(vs_row + (int64_t)j * sstride));
+      for (int j = lane; j < nk; j += 32) vmax = fmaxf(vmax, __ldg(vs_row + (int64_t)j * sstride));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
       v_ref = vmax > 0.f ? vmax : 1.f;
     }
     const float inv_vref = 1.f / v_ref;
     const int key_lim = CAUSAL ? min(ti.Lk, row + ti.Lk - ti.Lq + 1) : ti.Lk;
     float m_ref = NEG_INF, l = 0.f;
     bool ok = true;
+    // e4m3: the K and V scales of the next block are loaded one block ahead,
+    // so their latency is hidden behind this block's softmax
+    float ks_next = 0.f, vs_next = 0.f;
+    if (C::kFp8) {
+      ks_next = __ldg(ks_row + (int64_t)ti.kb0 * sstride);
+      vs_next = __ldg(vs_row + (int64_t)ti.kb0 * sstride);
+    }
     for (int i = 0; i < ti.n_kv; ++i, ++it) {
       const int kb = ti.kb0 + i;   // absolute 128-key block
-      const float c = C::kFp8 ? c_q * __ldg(ks_row + (int64_t)kb * sstride) : c_q;
+      const float ks_cur = ks_next, vs_cur = vs_next;
+      if (C::kFp8 && i + 1 < ti.n_kv) {
+        ks_next = __ldg(ks_row + (int64_t)(kb + 1) * sstride);
+        vs_next = __ldg(vs_row + (int64_t)(kb + 1) * sstride);
+      }
+      const float c = C::kFp8 ? c_q * ks_cur : c_q;
       // log2 of the factor the stored P carries: 2^kappa * v_s(j) / v_ref (e4m3 only)
-      const float lg_pw =
-          C::kFp8 ? ptx::lg2(__ldg(vs_row + (int64_t)kb * sstride) * inv_vref) + C::kLog2Kappa : 0.f;
+      const float lg_pw = C::kFp8 ? ptx::lg2(vs_cur * inv_vref) + C::kLog2Kappa : 0.f;
       const int buf = C::QT == 2 ? t : (int)(it & 1u);
       const uint32_t par = C::QT == 2 ? (it & 1u) : ((it >> 1) & 1u);
       if (!(ok = wt.wait_warp(bar(C::kBarSFull + buf), par, 6))) break;

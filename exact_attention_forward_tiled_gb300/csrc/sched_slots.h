@@ -1,15 +1,18 @@
 // Launch slots of the tile scheduler. Every persistent launch needs its own
 // pair of device counters {next tile, CTAs done} that start at zero; the
 // library keeps a fixed set of pairs per device (static __device__ arrays)
-// and the last CTA of a launch puts its pair back to zero. A slot may be
-// handed to a new launch only once the launch that last held it has
-// finished, or two launches would share counters and skip or repeat tiles.
+// and the last CTA of a launch puts its pair back to zero. Two launches that
+// run at the same time must never share a pair, or they would skip or repeat
+// tiles.
 //
-// SlotTable hands out slots in turn, skipping any still held, and returns
-// -1 when every slot is held by a launch in flight: the caller then refuses
-// the launch instead of reusing a live pair. Whether a launch has finished
-// is the caller's question to answer (a CUDA event query on the device, a
-// flag in the host test); plain host code, no CUDA types.
+// SlotTable hands out slots in turn, skipping any still held by a launch in
+// flight. When every slot is held it hands out the slot at `next` anyway --
+// the one handed out longest ago -- and says so (`wait` = true): the caller
+// must then order its launch after that slot's previous launch (an event
+// wait on its stream, done on the GPU), so that the two never run at once.
+// Whether a launch has finished is the caller's question to answer (a CUDA
+// event query on the device, a flag in the host test); plain host code, no
+// CUDA types.
 #pragma once
 
 namespace fa {
@@ -20,21 +23,35 @@ struct SlotTable {
   int next = 0;        // where the search for a free slot starts
 
   // The first slot from `next` on that is free: never handed out, or its
-  // launch finished (done(s) is true). -1 when all N are still held.
+  // launch finished (done(s) is true); wait = false. When all N are still
+  // held: the slot at `next`, still held by its previous launch, and
+  // wait = true.
   template <class Done>
-  int take(Done&& done) {
+  int take(Done&& done, bool& wait) {
     for (int k = 0; k < N; ++k) {
       const int s = (next + k) % N;
       if (!held[s] || done(s)) {
         held[s] = true;
         next = (s + 1) % N;
+        wait = false;
         return s;
       }
     }
-    return -1;
+    const int s = next;
+    next = (s + 1) % N;
+    wait = true;
+    return s;
   }
 
-  // The slot was handed out but nothing was launched with it.
+  // A slot for a launch that is not tracked (one captured into a graph):
+  // the slot at `next`, with no query and no change to what is held.
+  int untracked() {
+    const int s = next;
+    next = (s + 1) % N;
+    return s;
+  }
+
+  // A slot handed out free (wait = false) had nothing launched with it.
   void release(int s) {
     if (s >= 0 && s < N) held[s] = false;
   }

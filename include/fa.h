@@ -39,12 +39,17 @@
  *     after resetting it.
  *   - Concurrency: every kernel that schedules work tiles dynamically holds
  *     one of the device's 64 scheduler slots until it finishes (an event
- *     recorded after its launch says when). At most 64 such launches may be
- *     in flight on a device at once, over all streams and host threads; one
- *     more is refused with FA_ERR_BUSY and nothing is launched. A launch
- *     captured into a CUDA graph keeps the slot it was given at capture time
- *     for every replay, unseen by the library: replays must not overlap one
- *     another or other launches of the library on that device.
+ *     recorded after its launch says when). When all 64 are held by
+ *     launches in flight, over all streams and host threads, a new launch
+ *     reuses the slot handed out longest ago, and its stream first waits on
+ *     the GPU (cudaStreamWaitEvent) until that slot's previous launch has
+ *     finished: the call does not block the host, but with more than 64
+ *     launches in flight a launch may wait for one on another stream. A
+ *     launch captured into a CUDA graph is not tracked: it takes the next
+ *     slot in turn at capture time and keeps it for every replay, so
+ *     replays must not overlap one another or other launches of the library
+ *     on that device. FA_ERR_BUSY: the stream wait could not be issued;
+ *     nothing is launched.
  *   - The status word is per device, not per stream or call:
  *     fa_get_device_status() reports (and clears) what any kernel of the
  *     library on that device recorded since the last read.
@@ -67,7 +72,7 @@ extern "C" {
 #define FA_ERR_DEVICE_SEQLENS -6  /* a cu_seqlens entry broke its bounds       */
 #define FA_ERR_NO_DEVICE -7       /* no sm_100-family device is current        */
 #define FA_ERR_SCRATCH_LIMIT -8   /* needs more than the built-in scratch      */
-#define FA_ERR_BUSY -9            /* 64 launches already in flight on device   */
+#define FA_ERR_BUSY -9            /* no scheduler slot could be given          */
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
 
