@@ -258,6 +258,10 @@ int setup_fwd16(fa::FwdLaunch& L, DevInfo** devp, bool* nothing, const void* q, 
     *nothing = true;
     return FA_OK;
   }
+  // no keys at all: every row sees none, and the kernel's empty work tiles
+  // write O = 0 and LSE = -inf; K and V are never read, so (possibly null,
+  // as empty tensors are) their maps may point at O
+  if (Tk == 0) k = v = o;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -606,7 +610,10 @@ int fwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* q_
   const int64_t Tq = varlen ? total_q : (int64_t)B * Sq, Tk = varlen ? total_k : (int64_t)B * Sk;
   if (Tq > INT32_MAX || Tk > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (B == 0 || Sq == 0 || Tq == 0) return FA_OK;
-  if (!q8 || !k8 || !v8 || !o || !lse || !q_scale || (Sk > 0 && (!k_scale || !v_scale)))
+  // no keys at all: the empty work tiles write O = 0 and LSE = -inf and read
+  // neither K, V nor their scales, so (possibly null) K and V may point at O
+  if (Tk == 0) k8 = v8 = o;
+  if (!q8 || !k8 || !v8 || !o || !lse || !q_scale || (Tk > 0 && (!k_scale || !v_scale)))
     return FA_ERR_INVALID_ARG;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned4(lse) ||
       !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))

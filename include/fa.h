@@ -99,7 +99,11 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP8_E4M3 = 2 } fa_dtype;
  *                8-bit path is fa_fp8_prep + fa_fwd_fp8 below)
  *
  * A varlen sequence whose lengths break the bounds is skipped on the device
- * and reported as FA_ERR_DEVICE_SEQLENS by fa_get_device_status().
+ * and reported as FA_ERR_DEVICE_SEQLENS by fa_get_device_status(). A query
+ * row that sees no key (a sequence with no keys, or causal rows before the
+ * first visible key) gets O = 0 and LSE = -inf. With no key rows at all
+ * (Tk = 0), k and v are not read and may be NULL. With no query rows
+ * (B = 0, Sq = 0 or Tq = 0) the call does nothing and returns FA_OK.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Sq, int Sk, int D, float scale, int causal,
@@ -242,6 +246,8 @@ int fa_fp8_prep(const void* q, const void* k, const void* v, int in_dtype,
  *   D            64, 128 or 256 (at D = 64 a 64-byte row of codes is one
  *                TMA box in the 64-byte swizzle)
  *   scale, causal as for fa_fwd. Fixed length (varlen: fa_fwd_fp8_varlen).
+ *   Rows that see no key get O = 0 and LSE = -inf; with Sk = 0, k8, v8 and
+ *   their scales are not read and may be NULL.
  */
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
                const float* q_scale, const float* k_scale, const float* v_scale,

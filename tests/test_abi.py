@@ -61,6 +61,9 @@ def test_valid_call_without_gpu_reports_no_device(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _call(L) == -7
+    # no key rows at all: k and v may be NULL (the host checks pass)
+    assert _call(L, k=None, v=None, Sk=0) == -7
+    assert _call(L, k=None, Sk=128) == -1
     raw = ctypes.c_int(0)
     assert L.fa_get_device_status(None, ctypes.byref(raw)) == -7
 
