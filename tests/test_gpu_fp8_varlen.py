@@ -198,3 +198,39 @@ def test_fp8_varlen_bad_block_offsets_are_reported():
     assert st == -6, (st, raw)
     assert torch.equal(o[300:], o_ok[300:])
     assert int(o[:300].abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fp8_varlen_random_shapes(seed):
+    """Seeded draws of head size, causal mask, softmax scale (0.5 to 2 times
+    1/sqrt(D)), heads and per-sequence query / key lengths (empty ones
+    included): codes and scales bit for bit, attention element by element."""
+    r = np.random.default_rng(500 + seed)
+    D = int(r.choice([64, 128, 256]))
+    causal = bool(r.integers(2))
+    H = int(r.integers(1, 4))
+    n = int(r.integers(1, 6))
+    lq = [int(x) if r.random() > 0.15 else 0 for x in r.integers(1, 700, size=n)]
+    lk = [int(x) if r.random() > 0.15 else 0 for x in r.integers(1, 700, size=n)]
+    if sum(lq) == 0 or sum(lk) == 0:
+        lq[0], lk[0] = 77, 130
+    scale = float(r.uniform(0.5, 2.0)) * D ** -0.5
+    q = _rand((sum(lq), H, D), 600 + seed)
+    k = _rand((sum(lk), H, D), 700 + seed)
+    v = _rand((sum(lk), H, D), 800 + seed)
+    sigma = _sigma(D, 900 + seed)
+    cq, ck = _cu(lq), _cu(lk)
+    prep = api.fp8_prepare_varlen(q, k, v, sigma, cu_seqlens_q=cq, cu_seqlens_k=ck, max_seqlen_q=max(lq),
+                                  max_seqlen_k=max(lk))
+    o, lse = api.fp8_attention_forward(prep, causal=causal, scale=scale)
+    api.fa_get_device_status()
+    sg = sigma.cpu().numpy()
+    for name, x, lens, rot in (("q", q, lq, sg), ("k", k, lk, sg), ("v", v, lk, None)):
+        start = 0
+        for b, m in enumerate(lens):
+            for h in range(H):
+                ref_codes, ref_s = F.prepare(x[start:start + m, h, :].cpu(), rot)
+                codes, scales = _seq_head(prep, name, lens, b, h)
+                assert np.array_equal(scales, ref_s) and np.array_equal(codes, ref_codes), (name, b, h)
+            start += m
+    _check_seqs(prep, o, lse, lq, lk, H, scale, causal)
