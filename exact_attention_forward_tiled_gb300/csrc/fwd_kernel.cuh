@@ -74,12 +74,10 @@ struct FwdCfg {
   // lazy-rescale threshold (log2 units) and, for e4m3, the power of two P is
   // scaled by before it is rounded (P * 2^kappa <= 2^(tau + kappa) = 256 < 448)
   static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
-  // softmax arithmetic on packed fp32 pairs (fma/add .f32x2) or scalar
-  static constexpr bool kPacked = true;
-  // P handed to the MMA warp in two halves of 64 keys (e4m3, where the MMAs
-  // are short and the softmax is the critical path) or in one piece (16-bit,
-  // where the extra store round trip costs more than it saves)
-  static constexpr bool kSplitP = kFp8;
+  // P goes to the MMA warp in one piece. Handing e4m3 P over in two halves of
+  // 64 keys, so that the first half's products start while the second is
+  // made, bought nothing measurable (same box, c5 attention 1659 with halves
+  // against 1652 in one piece; c2 1494 against 1506 TFLOP/s)
   static constexpr float kKappaScale = kFp8 ? 16.0f : 1.0f;
   static constexpr float kLog2Kappa = kFp8 ? 4.0f : 0.0f;
   static constexpr int kSoftmaxWarps = 4 * QT;
@@ -120,12 +118,12 @@ struct FwdCfg {
   static constexpr int kOffBar = kOffEpi + (kTmaStore ? QT * kEpiBytes : 0);
   // barriers: q_full[2], q_empty[2] (per query tile, so the next work tile's
   // first Q tile loads while this one's last MMAs run), kv_full[S], kv_empty[S], s_full[2],
-  // p_full[2][2] (per score buffer, first / second half of the keys),
+  // p_full[2] (per score buffer),
   // o_full[2], pv_done, mma_done, tile_full[R], tile_empty[R]
   static constexpr int kTileRing = 4;   // work tiles fetched ahead by the load warp
   static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKVFull = 4, kBarKVEmpty = 4 + STAGES,
                        kBarSFull = 4 + 2 * STAGES, kBarPFull = kBarSFull + 2,
-                       kBarOFull = kBarPFull + 4, kBarPVDone = kBarOFull + 2,
+                       kBarOFull = kBarPFull + 2, kBarPVDone = kBarOFull + 2,
                        kBarMmaDone = kBarPVDone + 1, kBarTileFull = kBarMmaDone + 1,
                        kBarTileEmpty = kBarTileFull + kTileRing, kNumBars = kBarTileEmpty + kTileRing;
   // MMA thread + one lane per softmax warp (+ the V-load warp with paged K/V)
@@ -451,15 +449,12 @@ __device__ void mma_role(const FwdParams& p, uint32_t sbase, uint32_t tmem, cons
     }
   };
   // O[o_col] (+)= P[p_col] V : steps of kKeysPerStep keys; 8 P columns per
-  // step. P arrives in two halves (keys 0-63, 64-127), each with its own
-  // barrier, so the first half's MMAs start while the second half is made.
+  // step, once P of score buffer pbuf is in tensor memory
   auto pv = [&](uint32_t o_col, uint32_t p_col, uint32_t v_addr, bool acc, int pbuf, uint32_t parity) -> bool {
+    if (!wt.wait(bar(C::kBarPFull + pbuf), parity, 5)) return false;
+    ptx::tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < C::kPvSteps; ++kk) {
-      if (kk == 0 || (C::kSplitP && kk == C::kPvSteps / 2)) {
-        if (!wt.wait(bar(C::kBarPFull + 2 * pbuf + (kk == 0 ? 0 : 1)), parity, 5)) return false;
-        ptx::tc_fence_after();
-      }
       const uint64_t b = ptx::smem_desc_sw<C::kRowBytes>(v_addr + kk * C::kKeysPerStep * C::kRowBytes,
                                                          C::kBoxBytes, 8 * C::kRowBytes);
       const uint32_t en = (acc || kk > 0) ? 1u : 0u;
@@ -745,8 +740,8 @@ __device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t
         }
       }
       // exponent argument s * c - m (+ log2 of the e4m3 P weight), two lanes
-      // at a time; P goes out in two halves of 64 keys, each released to the
-      // MMA warp as soon as it sits in tensor memory; the row sum comes after
+      // at a time, in two halves of 64 keys; P goes to the MMA warp once both
+      // sit in tensor memory; the row sum comes after
       const float mu = (m_ref == NEG_INF ? 0.f : m_ref) - lg_pw;
       const uint64_t c2 = ptx::f2pack(c, c), nm2 = ptx::f2pack(-mu, -mu);
 #pragma unroll
@@ -754,12 +749,7 @@ __device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t
 #pragma unroll
         for (int j = 64 * hf; j < 64 * hf + 64; j += 2) {
           float lo, hi;
-          if (C::kPacked) {
-            ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
-          } else {
-            lo = fmaf(s[j], c, -mu);
-            hi = fmaf(s[j + 1], c, -mu);
-          }
+          ptx::f2unpack(ptx::fma2(ptx::f2pack(s[j], s[j + 1]), c2, nm2), lo, hi);
           s[j] = ptx::ex2(lo);
           s[j + 1] = ptx::ex2(hi);
         }
@@ -783,31 +773,22 @@ __device__ void softmax_role(const FwdParams& p, const CUtensorMap* to, uint32_t
           for (int j = 0; j < 32; ++j) pk[j] = pack_p16<C::KIND>(s[64 * hf + 2 * j], s[64 * hf + 2 * j + 1]);
           ptx::tmem_st32(s_addr + 32 * hf, pk);
         }
-        if (C::kSplitP || hf == 1) {
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + 2 * buf + (C::kSplitP ? hf : 0)));
-        }
       }
-      float tile_sum;
-      if (C::kPacked) {
-        uint64_t acc[4] = {0, 0, 0, 0};
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + buf));
+      // the row sum, on packed pairs: pair j / 2 goes to acc[(j / 2) % 4]
+      uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int j = 0; j < 128; j += 2)
-          acc[(j >> 1) & 3] = ptx::add2(acc[(j >> 1) & 3], ptx::f2pack(s[j], s[j + 1]));
-        float a0, a1, b0, b1, c0, c1, d0, d1;
-        ptx::f2unpack(acc[0], a0, a1);
-        ptx::f2unpack(acc[1], b0, b1);
-        ptx::f2unpack(acc[2], c0, c1);
-        ptx::f2unpack(acc[3], d0, d1);
-        tile_sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-      } else {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j & 7] += s[j];
-        tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      }
+      for (int j = 0; j < 128; j += 2)
+        acc[(j >> 1) & 3] = ptx::add2(acc[(j >> 1) & 3], ptx::f2pack(s[j], s[j + 1]));
+      float a0, a1, b0, b1, c0, c1, d0, d1;
+      ptx::f2unpack(acc[0], a0, a1);
+      ptx::f2unpack(acc[1], b0, b1);
+      ptx::f2unpack(acc[2], c0, c1);
+      ptx::f2unpack(acc[3], d0, d1);
+      const float tile_sum = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
       {
         // e4m3: the stored P carries the weight 2^lg_pw; l sums unweighted P
         l += C::kFp8 ? tile_sum * ptx::ex2(-lg_pw) : tile_sum;
@@ -925,7 +906,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT, STAGES, KIND>::kThreads, 1)
     const uint32_t bars = sbase + C::kOffBar;
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
-      if (i >= C::kBarPFull && i < C::kBarPFull + 4) count = 4;
+      if (i >= C::kBarPFull && i < C::kBarPFull + 2) count = 4;
       if (i >= C::kBarTileEmpty) count = C::kTileConsumers + (p.block_table != nullptr ? 1 : 0);
       ptx::mbar_init(bars + 8u * i, count);
     }
