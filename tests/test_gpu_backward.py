@@ -258,3 +258,25 @@ def test_backward_extreme_scales(scale):
             assert (err <= 2.0 * bd + 1e-6).all(), (name, h, float(err.max()))
     if scale == 0.0:
         assert int(dq.abs().sum().item()) == 0 and int(dk.abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_backward_random_shapes(seed):
+    """Seeded draws of input type, head size, causal mask and fixed or varlen
+    shapes (empty sequences included), every element within the bound."""
+    r = np.random.default_rng(7000 + seed)
+    dtype = [torch.float16, torch.bfloat16][r.integers(2)]
+    D = int(r.choice([64, 128, 256]))
+    causal = bool(r.integers(2))
+    H = int(r.integers(1, 3))
+    if r.integers(2):
+        n = int(r.integers(1, 5))
+        lq = [int(x) if r.random() > 0.15 else 0 for x in r.integers(1, 500, size=n)]
+        lk = [int(x) if r.random() > 0.15 else 0 for x in r.integers(1, 500, size=n)]
+        if sum(lq) == 0 or sum(lk) == 0:
+            lq[0], lk[0] = 200, 137
+        _check(None, H, max(lq), max(lk), D, causal, dtype, 7100 + 10 * seed, lq=lq, lk=lk)
+    else:
+        B = int(r.integers(1, 3))
+        Sq, Sk = (int(x) for x in r.integers(1, 500, size=2))
+        _check(B, H, Sq, Sk, D, causal, dtype, 7100 + 10 * seed)
