@@ -182,3 +182,42 @@ def test_paged_key_ranges_with_several_queries():
     api.fa_get_device_status()
     o_ref, lse_ref = _oracle(q, k, v, lens, Sq, D ** -0.5, True)
     _check_vs_oracle(o, lse, o_ref, lse_ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_paged_random_shapes(seed):
+    """Seeded draws of page size, head size, mask, query length and per-
+    sequence key lengths (empty ones included): the oracle's bars, and bit
+    equality with the contiguous varlen path on the gathered keys."""
+    r = np.random.default_rng(9000 + seed)
+    page_size = int(r.choice([16, 32, 64, 128, 256]))
+    D = int(r.choice([64, 128, 256]))
+    causal = bool(r.integers(2))
+    H = int(r.integers(1, 3))
+    n = int(r.integers(1, 6))
+    lens = [int(x) if r.random() > 0.15 else 0 for x in r.integers(1, 900, size=n)]
+    if sum(lens) == 0:
+        lens[0] = 333
+    Sq = int(r.integers(1, 200))
+    dtype = [torch.float16, torch.bfloat16][r.integers(2)]
+    q, k, v, kc, vc, table, seqlens = _paged_problem(lens, Sq, H, D, page_size, dtype, seed=9100 + seed)
+    o, lse = api.attention_forward_paged(q, kc, vc, table, seqlens, causal=causal)
+    api.fa_get_device_status()
+    o_ref, lse_ref = _oracle(q, k, v, lens, Sq, D ** -0.5, causal)
+    # the 16-bit bar plus one unit of the output type's rounding times |O_ref|
+    # (rows that see one or two keys have |O| near max |V|)
+    rel = 2.0 ** -11 if dtype == torch.float16 else 2.0 ** -8
+    err = np.abs(o.float().cpu().numpy() - o_ref)
+    assert (err / (TOL_O[dtype] + rel * np.abs(o_ref))).max() <= 1.0
+    l = lse.cpu().numpy()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(l), fin)
+    if fin.any():
+        assert np.abs(l[fin] - lse_ref[fin]).max() <= 1e-3
+    cq = torch.arange(len(lens) + 1, dtype=torch.int32, device="cuda") * Sq
+    ck = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    o2, lse2 = api.attention_forward(q, k, v, causal=causal, cu_seqlens_q=cq, cu_seqlens_k=ck, max_seqlen_q=Sq,
+                                     max_seqlen_k=max(lens))
+    api.fa_get_device_status()
+    assert torch.equal(o, o2)
+    assert torch.equal(lse, lse2.reshape(H, len(lens), Sq).permute(1, 0, 2))
